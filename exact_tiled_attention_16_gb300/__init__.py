@@ -1,0 +1,19 @@
+"""Exact tiled attention forward pass for one GB300 (sm_103a).
+
+The compute path is the shared library built from ``csrc/`` (``libattn.so``):
+hand-written tcgen05/TMA kernels behind a C ABI (``include/attn.h``).  This
+package only marshals arguments into that library; it has no CPU fallback.
+
+``synth`` (seeded input generation) imports without the library.  The binding
+functions load the library on first use and raise if it is missing.
+"""
+from __future__ import annotations
+
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_status_string", "load_library", "AttnError"]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import _lib
+        return getattr(_lib, name)
+    raise AttributeError(name)

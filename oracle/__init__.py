@@ -1,0 +1,6 @@
+"""fp64 CPU oracle for exact attention (test infrastructure only).
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
+this package.  The library's compute path never calls it.
+"""
+from .attention import attention_head, attention, attention_probs  # noqa: F401
