@@ -1,0 +1,114 @@
+"""ctypes binding of libattn.so (argument marshalling only).
+
+Every step of the attention computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or the device is not sm_103,
+the calls raise AttnError.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_OK = 0
+ATTN_BF16 = 0
+ATTN_ERR_TIMEOUT = -8
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {attn_status_string(status)} ({status})" if what else attn_status_string(status))
+
+
+def load_library():
+    """Loads libattn.so (built by exact_tiled_attention_16_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m exact_tiled_attention_16_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
+    lib.attn_fwd.restype = ci
+    lib.attn_status_string.argtypes = [ci]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_check_device_errors.argtypes = [vp, ctypes.POINTER(ci)]
+    lib.attn_check_device_errors.restype = ci
+    lib.attn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+    lib.attn_set_wait_timeout_ns.restype = ci
+    lib.attn_selftest_wait_timeout.argtypes = [vp]
+    lib.attn_selftest_wait_timeout.restype = ci
+    _lib = lib
+    return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def attn_fwd_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int, causal: bool,
+                 scale: float, stream: int, dtype: int = ATTN_BF16) -> int:
+    """Direct call with device pointers; returns the attn_status."""
+    return load_library().attn_fwd(q or None, k or None, v or None, o or None, lse or None, B, H, N, d,
+                                   1 if causal else 0, float(scale), dtype, stream or None)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+             want_lse: bool = True, stream=None):
+    """Exact attention forward for torch CUDA tensors q, k, v [B,H,N,d] bf16.
+
+    Returns (o, lse); o is bf16 [B,H,N,d], lse float32 [B,H,N] (None if
+    want_lse is False and no lse buffer was given).  Output buffers may be passed
+    in to avoid allocation.  Asynchronous on `stream` (default: torch's current
+    stream)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [B,H,N,d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape [B,H,N,d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                      lse.data_ptr() if lse is not None else 0, B, H, N, d, causal, scale,
+                      _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def check_device_errors(stream=None):
+    """Synchronises the stream and returns (status, where) of the device error word."""
+    where = ctypes.c_int(0)
+    rc = load_library().attn_check_device_errors(_stream_handle(stream) or None, ctypes.byref(where))
+    return rc, where.value
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    return load_library().attn_set_wait_timeout_ns(int(ns))
+
+
+def selftest_wait_timeout(stream=None) -> int:
+    return load_library().attn_selftest_wait_timeout(_stream_handle(stream) or None)

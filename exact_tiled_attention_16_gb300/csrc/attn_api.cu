@@ -1,0 +1,233 @@
+// C ABI of the attention library: argument validation, TMA tensor-map encoding,
+// per-device set-up and kernel launches.  See include/attn.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+using namespace attn;
+
+// Device error word: a kernel that gives up on a bounded wait writes
+// (where << 8) | kDevErrTimeout here (first failure wins).
+__device__ int g_attn_err = 0;
+
+unsigned long long g_timeout_ns = 4000000000ull;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int status = ATTN_ERR_CUDA;
+  int num_sms = 0;
+  int* err_ptr = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+template <int D, int NSTAGE>
+cudaError_t configure_bf16() {
+  return cudaFuncSetAttribute(attn_fwd_bf16_kernel<D, NSTAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fwd_smem_bytes<D, NSTAGE>()));
+}
+
+constexpr int kStages64 = 4;
+constexpr int kStages128 = 2;
+
+// Per-device set-up on first use: architecture check, SM count, kernel
+// attributes, address of the error word.  Returns ATTN_OK or an error status.
+int device_setup(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&st, dev] {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      st.status = ATTN_ERR_CUDA;
+      return;
+    }
+    if (major != 10 || minor != 3) {
+      st.status = ATTN_ERR_ARCH;
+      return;
+    }
+    if (configure_bf16<64, kStages64>() != cudaSuccess || configure_bf16<128, kStages128>() != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_ptr), g_attn_err) != cudaSuccess) {
+      st.status = ATTN_ERR_CUDA;
+      return;
+    }
+    st.status = ATTN_OK;
+  });
+  *dev_out = dev;
+  return st.status;
+}
+
+// 3-D tiled map over a contiguous [BH, N, d] tensor: dims (d, N, BH), box
+// (box_inner elements, 128 rows, 1), 128-byte swizzle, zero fill out of bounds.
+int make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, uint32_t elem_bytes, int d, int N,
+             int BH, uint32_t box_inner) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return ATTN_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
+                           static_cast<cuuint64_t>(d) * elem_bytes * static_cast<cuuint64_t>(N)};
+  cuuint32_t box[3] = {box_inner, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_OVERFLOW;
+}
+
+int validate_common(const void* q, const void* k, const void* v, const void* o, const void* lse, int B, int H,
+                    int N, int d, float scale) {
+  if (!q || !k || !v || !o) return ATTN_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_DIMS;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                      reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if (a & 15u) return ATTN_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_ALIGN;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long qblocks = (static_cast<long long>(N) + kBlockM - 1) / kBlockM;
+  if (BH > INT_MAX || BH * qblocks > INT_MAX) return ATTN_ERR_OVERFLOW;
+  // TMA global strides must stay below 2^40 bytes.
+  if (static_cast<long long>(N) * d * 2 >= (1ll << 40)) return ATTN_ERR_OVERFLOW;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             int causal, float scale, int dtype, void* stream) {
+  int rc = validate_common(q, k, v, o, lse, B, H, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
+  if ((rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
+  if ((rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
+
+  FwdParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = BH;
+  p.N = N;
+  p.num_qblocks = (N + kBlockM - 1) / kBlockM;
+  p.num_units = BH * p.num_qblocks;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.err = g_dev[dev].err_ptr;
+
+  const int grid = p.num_units < g_dev[dev].num_sms ? p.num_units : g_dev[dev].num_sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 64) {
+    attn_fwd_bf16_kernel<64, kStages64>
+        <<<grid, kNumThreads, fwd_smem_bytes<64, kStages64>(), s>>>(mq, mk, mv, p);
+  } else {
+    attn_fwd_bf16_kernel<128, kStages128>
+        <<<grid, kNumThreads, fwd_smem_bytes<128, kStages128>(), s>>>(mq, mk, mv, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_NULL: return "ATTN_ERR_NULL: a required pointer is NULL";
+    case ATTN_ERR_DIMS: return "ATTN_ERR_DIMS: B, H and N must be >= 1";
+    case ATTN_ERR_UNSUPPORTED_HEADDIM: return "ATTN_ERR_UNSUPPORTED_HEADDIM: d must be 64 or 128";
+    case ATTN_ERR_DTYPE: return "ATTN_ERR_DTYPE: unknown dtype";
+    case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: tensors must be 16-byte aligned (lse/scales 4-byte)";
+    case ATTN_ERR_OVERFLOW: return "ATTN_ERR_OVERFLOW: sizes exceed 32-bit work indexing or TMA limits";
+    case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH: kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+    case ATTN_ERR_ARCH: return "ATTN_ERR_ARCH: the current device is not sm_103";
+    case ATTN_ERR_SCALE: return "ATTN_ERR_SCALE: scale must be finite and > 0";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA call failed (no device?)";
+    default: return "unknown attn_status";
+  }
+}
+
+int attn_check_device_errors(void* stream, int* where_out) {
+  int dev = 0;
+  int rc = device_setup(&dev);
+  if (rc != ATTN_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int word = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_attn_err, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_attn_err, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (where_out) *where_out = word >> 8;
+  return (word & 0xff) == kDevErrTimeout ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+int attn_set_wait_timeout_ns(unsigned long long ns) {
+  if (ns < 1000ull) return ATTN_ERR_DIMS;
+  g_timeout_ns = ns;
+  return ATTN_OK;
+}
+
+}  // extern "C"
+
+namespace {
+// One CTA waits on an mbarrier that nothing ever arrives at; the bounded wait
+// must give up, record the timeout and let the kernel exit normally.
+__global__ void wait_selftest_kernel(unsigned long long timeout_ns, int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_word;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_word = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(smem_u32(&bar), 0, &abort_word, timeout_ns, err, 99);
+}
+}  // namespace
+
+extern "C" int attn_selftest_wait_timeout(void* stream) {
+  int dev = 0;
+  int rc = device_setup(&dev);
+  if (rc != ATTN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  wait_selftest_kernel<<<1, 32, 0, s>>>(g_timeout_ns, g_dev[dev].err_ptr);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return attn_check_device_errors(stream, nullptr);
+}

@@ -1,0 +1,103 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact attention forward pass on one NVIDIA
+ * GB300 (sm_103a).
+ *
+ * Operation (the standard scaled dot-product attention that FlashAttention-2
+ * reproduces exactly: FlashAttention-2 article, introduction and "Background";
+ * computed tile by tile with the online softmax of the ring-attention page,
+ * "technical insight", and the deferred rescaling of the news article
+ * "FlashAttention scaling, multi-GPU training and weight quantisation", section 1):
+ *
+ *   for every batch b, head h and query row i:
+ *     s_ij   = scale * sum_c q[b,h,i,c] * k[b,h,j,c]      (j = 0 .. N-1)
+ *     causal: s_ij = -inf for j > i   (square mask, top-left aligned)
+ *     o[b,h,i,:] = sum_j softmax_j(s_i.) * v[b,h,j,:]
+ *     lse[b,h,i] = ln sum_j exp(s_ij)                     (natural log)
+ *
+ * Layouts: q, k, v, o are contiguous [B, H, N, d] (row-major, d fastest);
+ * lse is contiguous [B, H, N] float32.
+ *
+ * Ownership and synchronisation: the caller owns every buffer (device memory)
+ * and the stream.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream); o and lse are valid once the stream has reached
+ * the end of the call.  The library allocates no device memory per call and
+ * keeps only per-device cached properties and kernel attributes.
+ *
+ * Errors: arguments are validated before anything is launched; a failed check
+ * returns a negative attn_status and launches nothing.  A failure to launch
+ * returns ATTN_ERR_LAUNCH.  Inside the kernels every wait on another warp or on
+ * a copy engine is bounded (attn_set_wait_timeout_ns); a wait that runs out
+ * records ATTN_ERR_TIMEOUT in a device error word, which
+ * attn_check_device_errors() reports.  There is no CPU fallback: without an
+ * sm_103 device the calls return ATTN_ERR_ARCH or ATTN_ERR_CUDA.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = -1,                /* a required pointer is NULL */
+  ATTN_ERR_DIMS = -2,                /* B, H or N < 1 */
+  ATTN_ERR_UNSUPPORTED_HEADDIM = -3, /* d not in {64, 128} */
+  ATTN_ERR_DTYPE = -4,               /* dtype not an attn_dtype value */
+  ATTN_ERR_ALIGN = -5,               /* q/k/v/o not 16-byte aligned, or lse/scales not 4-byte aligned */
+  ATTN_ERR_OVERFLOW = -6,            /* sizes exceed the 32-bit work indexing or TMA limits */
+  ATTN_ERR_LAUNCH = -7,              /* the kernel launch failed */
+  ATTN_ERR_TIMEOUT = -8,             /* a bounded in-kernel wait ran out (see attn_check_device_errors) */
+  ATTN_ERR_ARCH = -9,                /* the current device is not sm_103 */
+  ATTN_ERR_SCALE = -10,              /* scale not finite and > 0 */
+  ATTN_ERR_CUDA = -11                /* a CUDA runtime/driver call failed (e.g. no device) */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0 } attn_dtype;
+
+/*
+ * attn_fwd -- BF16 exact attention forward.
+ *   q, k, v : const bf16 [B,H,N,d], 16-byte aligned device pointers
+ *   o       : bf16 [B,H,N,d] output, 16-byte aligned
+ *   lse     : float32 [B,H,N] output, 4-byte aligned; may be NULL (not written)
+ *   B, H, N : >= 1;  d : 64 or 128
+ *   causal  : 0 = no mask, nonzero = key j visible to query i iff j <= i
+ *   scale   : finite, > 0 (usually 1/sqrt(d))
+ *   dtype   : ATTN_BF16
+ *   stream  : cudaStream_t
+ * Arithmetic: bf16 Q K^T and P V on the tensor cores with fp32 accumulation,
+ * softmax in fp32 with P rounded to bf16, O rounded to bf16 (nearest-even).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             int causal, float scale, int dtype, void* stream);
+
+/* Human-readable name of an attn_status value (static storage). */
+const char* attn_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up on a bounded
+ * wait since the last check (*where_out, if not NULL, receives the code of the
+ * wait that gave up), or ATTN_ERR_CUDA.
+ */
+int attn_check_device_errors(void* stream, int* where_out);
+
+/*
+ * Sets the limit of every in-kernel wait launched afterwards (nanoseconds,
+ * >= 1000; default 4e9).  Returns ATTN_OK or ATTN_ERR_DIMS.
+ */
+int attn_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * Self-test of the bounded wait: launches one CTA that waits on an mbarrier
+ * nobody arrives at, with the current wait limit.  The kernel gives up, records
+ * the timeout and exits; the call synchronises `stream` and returns what
+ * attn_check_device_errors returns (ATTN_ERR_TIMEOUT when the wait is working).
+ */
+int attn_selftest_wait_timeout(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -1,0 +1,64 @@
+"""Helpers shared by the GPU tests: upload seeded workloads, run the library,
+compare with the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+from exact_tiled_attention_16_gb300 import synth
+from oracle.attention import attention_head
+
+# Tolerances for the BF16 path against the fp64 oracle on the same bf16 inputs.
+BF16_MAX_ABS_O = 2e-2
+BF16_MEAN_ABS_O = 2e-3
+BF16_MAX_ABS_LSE = 1e-3
+
+
+def to_device(w: synth.Workload, dev="cuda"):
+    import torch
+    if w.dtype == "bf16":
+        return tuple(torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+                     for x in (w.q, w.k, w.v))
+    return tuple(torch.from_numpy(np.ascontiguousarray(x)).to(dev) for x in (w.q, w.k, w.v))
+
+
+def run_bf16(w: synth.Workload, dev="cuda", want_lse=True):
+    import torch
+    import exact_tiled_attention_16_gb300 as pkg
+    q, k, v = to_device(w, dev)
+    o, lse = pkg.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, want_lse=want_lse)
+    torch.cuda.synchronize()
+    rc, where = pkg.check_device_errors()
+    assert rc == 0, f"device error word set by wait {where}"
+    o_np = o.float().cpu().numpy().astype(np.float64)
+    lse_np = lse.cpu().numpy().astype(np.float64) if lse is not None else None
+    return o_np, lse_np
+
+
+def compare_rows(w: synth.Workload, o_np, lse_np, rows_per_head=None, seed_rows=0):
+    """Compares the GPU result with the oracle on all rows (rows_per_head None)
+    or on a seeded sample of rows per head.  Returns (max|dO|, mean|dO|, max|dLSE|)."""
+    max_o = 0.0
+    sum_o = 0.0
+    cnt = 0
+    max_l = 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            q, k, v = w.head_f64(b, h)
+            rows = None if rows_per_head is None else synth.sample_rows(w.N, rows_per_head, w.seed + seed_rows, b, h)
+            ro, rl = attention_head(q, k, v, w.causal, w.scale, rows=rows)
+            go = o_np[b, h] if rows is None else o_np[b, h][rows]
+            d = np.abs(go - ro)
+            max_o = max(max_o, float(d.max()))
+            sum_o += float(d.sum())
+            cnt += d.size
+            if lse_np is not None:
+                gl = lse_np[b, h] if rows is None else lse_np[b, h][rows]
+                max_l = max(max_l, float(np.abs(gl - rl).max()))
+    return max_o, sum_o / cnt, max_l
+
+
+def assert_bf16_tol(stats, what=""):
+    max_o, mean_o, max_l = stats
+    assert max_o <= BF16_MAX_ABS_O, f"{what} max|dO| {max_o:.4g} > {BF16_MAX_ABS_O}"
+    assert mean_o <= BF16_MEAN_ABS_O, f"{what} mean|dO| {mean_o:.4g} > {BF16_MEAN_ABS_O}"
+    assert max_l <= BF16_MAX_ABS_LSE, f"{what} max|dLSE| {max_l:.4g} > {BF16_MAX_ABS_LSE}"

@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports every symbol include/attn.h
+declares; argument validation returns the documented codes before any CUDA
+call (no GPU needed for these)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_tiled_attention_16_gb300 import build as b
+    b.build()
+    import exact_tiled_attention_16_gb300._lib as L
+    return L.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_status_string", "attn_check_device_errors"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    nm = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True)
+    exported = set(re.findall(r"\sT\s+(\w+)$", nm.stdout, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, f"{name} declared in include/ but not exported"
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    import exact_tiled_attention_16_gb300._lib as L
+    assert L.attn_status_string(0) == "ATTN_OK"
+    for code in range(-11, 0):
+        assert L.attn_status_string(code).startswith("ATTN_ERR_")
+    assert "unknown" in L.attn_status_string(-999)
+
+
+def _call(lib, q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=128, d=64, causal=0,
+          scale=0.125, dtype=0):
+    import exact_tiled_attention_16_gb300._lib as L
+    return L.attn_fwd_raw(q, k, v, o, lse, B, H, N, d, causal, scale, 0, dtype)
+
+
+# Cases rejected by host-side validation, before any CUDA call or launch.
+INVALID = [
+    (dict(q=0), -1), (dict(k=0), -1), (dict(v=0), -1), (dict(o=0), -1),
+    (dict(B=0), -2), (dict(H=-1), -2), (dict(N=0), -2),
+    (dict(d=32), -3), (dict(d=96), -3), (dict(d=256), -3),
+    (dict(scale=0.0), -10), (dict(scale=-1.0), -10), (dict(scale=float("inf")), -10),
+    (dict(scale=float("nan")), -10),
+    (dict(q=0x1008), -5), (dict(o=0x4004), -5), (dict(lse=0x5002), -5),
+    (dict(B=1 << 16, H=1 << 16), -6),
+    (dict(dtype=7), -4),
+]
+
+
+@pytest.mark.parametrize("kwargs,code", INVALID, ids=[str(c[0]) for c in INVALID])
+def test_validation_codes(lib, kwargs, code):
+    assert _call(lib, **kwargs) == code
+
+
+def test_wait_timeout_setter(lib):
+    assert lib.attn_set_wait_timeout_ns(10) == -2
+    assert lib.attn_set_wait_timeout_ns(4_000_000_000) == 0
+
+
+def test_no_device_fails_loudly(lib):
+    """Without a GPU the valid call reports a CUDA error: nothing falls back to the CPU."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a device is present; this checks the no-device path")
+    assert _call(lib) == -11
+
+
+def test_binding_raises_without_library(tmp_path, monkeypatch):
+    import exact_tiled_attention_16_gb300._lib as L
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(L, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        L.load_library()

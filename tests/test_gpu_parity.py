@@ -1,0 +1,188 @@
+"""GPU parity of the BF16 attention forward (through the C ABI) against the fp64
+oracle on the same seeded inputs.
+
+Tolerances (bf16 inputs, fp32 accumulation, bf16 P and O):
+max|dO| <= 2e-2, mean|dO| <= 2e-3, max|dLSE| <= 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from exact_tiled_attention_16_gb300 import synth
+from tests.gpu_utils import assert_bf16_tol, compare_rows, run_bf16, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_tiled_attention_16_gb300 as pkg
+    pkg.load_library()
+
+
+SMALL = [
+    # (B, H, N, d): single tile, ragged tails, several tiles
+    (1, 1, 1, 64), (1, 1, 7, 128), (1, 2, 128, 64), (2, 1, 129, 128), (1, 3, 200, 64),
+    (1, 1, 257, 128), (2, 2, 384, 64), (1, 2, 1000, 128), (3, 5, 640, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=[f"B{b}H{h}N{n}d{d}" for b, h, n, d in SMALL])
+def test_small_full_oracle(shape, causal):
+    B, H, N, d = shape
+    w = synth.make_bf16(B, H, N, d, causal, seed=100 + N + d)
+    o, lse = run_bf16(w)
+    assert_bf16_tol(compare_rows(w, o, lse), f"{shape} causal={causal}")
+
+
+def test_cfg1_full():
+    w = synth.make_config("cfg1")
+    o, lse = run_bf16(w)
+    assert_bf16_tol(compare_rows(w, o, lse), "cfg1")
+
+
+@pytest.mark.parametrize("name", ["cfg2n", "cfg2c"])
+def test_cfg2_full(name):
+    w = synth.make_config(name)
+    o, lse = run_bf16(w)
+    assert_bf16_tol(compare_rows(w, o, lse), name)
+
+
+@pytest.mark.parametrize("name", ["cfg3", "cfg4"])
+def test_large_config_sampled_rows(name):
+    w = synth.make_config(name)
+    o, lse = run_bf16(w)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert_bf16_tol(compare_rows(w, o, lse, rows_per_head=256), name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_sampled(causal):
+    """A single long head: many K/V blocks and, causal, the heaviest tiles."""
+    w = synth.make_bf16(1, 1, 65536 + 77, 128, causal, seed=21)
+    o, lse = run_bf16(w)
+    assert_bf16_tol(compare_rows(w, o, lse, rows_per_head=256), "N=65613")
+
+
+def test_deterministic_bitwise():
+    w = synth.make_bf16(2, 4, 1500, 128, True, seed=9)
+    q, k, v = to_device(w)
+    import exact_tiled_attention_16_gb300 as pkg
+    o1, l1 = pkg.attn_fwd(q, k, v, causal=True, scale=w.scale)
+    o2, l2 = pkg.attn_fwd(q, k, v, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_causal_last_row_equals_noncausal():
+    wc = synth.make_bf16(1, 4, 1024, 128, True, seed=31)
+    wn = synth.make_bf16(1, 4, 1024, 128, False, seed=31)
+    oc, lc = run_bf16(wc)
+    on, ln_ = run_bf16(wn)
+    np.testing.assert_array_equal(oc[:, :, -1], on[:, :, -1])
+    np.testing.assert_array_equal(lc[:, :, -1], ln_[:, :, -1])
+    # causal row 0 is v0 (rounded to bf16 twice at most)
+    v0 = synth.bf16_bits_to_f64(wc.v[:, :, 0])
+    np.testing.assert_allclose(oc[:, :, 0], v0, atol=1e-2, rtol=1e-2)
+
+
+def test_invariants_on_gpu():
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d = 1, 2, 700, 64
+    w = synth.make_bf16(B, H, N, d, False, seed=41)
+    q, k, v = to_device(w)
+    # constant V -> constant O
+    vc = torch.full_like(v, 1.5)
+    for causal in (False, True):
+        o, _ = pkg.attn_fwd(q, k, vc, causal=causal)
+        torch.cuda.synchronize()
+        assert (o.float() - 1.5).abs().max().item() <= 1.5 * 1e-2
+    # Q = 0 -> mean of the visible V rows, lse = ln(#visible)
+    qz = torch.zeros_like(q)
+    for causal in (False, True):
+        o, lse = pkg.attn_fwd(qz, k, v, causal=causal, scale=0.3)
+        torch.cuda.synchronize()
+        vf = v.double()
+        if causal:
+            ref = vf.cumsum(dim=2) / torch.arange(1, N + 1, device=vf.device, dtype=vf.dtype)[None, None, :, None]
+            nvis = torch.arange(1, N + 1, device=vf.device, dtype=torch.float64)
+        else:
+            ref = vf.mean(dim=2, keepdim=True).expand_as(vf)
+            nvis = torch.full((N,), float(N), device=vf.device, dtype=torch.float64)
+        assert (o.double() - ref).abs().max().item() <= 2e-2
+        assert (lse.double() - nvis.log()[None, None]).abs().max().item() <= 1e-3
+
+
+def test_lse_optional():
+    w = synth.make_bf16(1, 2, 300, 128, True, seed=51)
+    o1, l1 = run_bf16(w)
+    o2, l2 = run_bf16(w, want_lse=False)
+    assert l2 is None
+    np.testing.assert_array_equal(o1, o2)
+
+
+def test_no_writes_outside_outputs():
+    """O and LSE are written in place inside guard regions that must stay intact."""
+    import exact_tiled_attention_16_gb300._lib as L
+    B, H, N, d = 1, 3, 333, 64
+    w = synth.make_bf16(B, H, N, d, True, seed=61)
+    q, k, v = to_device(w)
+    guard = 4096
+    o_buf = torch.full((B * H * N * d + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * N + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+    o_view = o_buf[guard:guard + B * H * N * d]
+    l_view = l_buf[guard:guard + B * H * N]
+    rc = L.attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_view.data_ptr(), l_view.data_ptr(),
+                        B, H, N, d, True, w.scale, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.isnan(o_buf[:guard].float()).all() and torch.isnan(o_buf[-guard:].float()).all()
+    assert torch.isnan(l_buf[:guard]).all() and torch.isnan(l_buf[-guard:]).all()
+    assert not torch.isnan(o_view.float()).any() and not torch.isnan(l_view).any()
+    assert_bf16_tol(compare_rows(w, o_view.view(B, H, N, d).float().cpu().numpy().astype(np.float64),
+                                 l_view.view(B, H, N).cpu().numpy().astype(np.float64)), "guarded")
+
+
+def test_invalid_arguments_launch_nothing():
+    import exact_tiled_attention_16_gb300._lib as L
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device="cuda")
+    o = torch.full_like(q, 7.0)
+    s = torch.cuda.current_stream().cuda_stream
+    assert L.attn_fwd_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), 0, 1, 1, 128, 96, 0, 0.1, s) == -3
+    assert L.attn_fwd_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), 0, 1, 1, 128, 64, 0, -1.0, s) == -10
+    torch.cuda.synchronize()
+    assert (o.float() == 7.0).all()
+
+
+def test_bounded_wait_selftest():
+    """A wait that nobody satisfies gives up with ATTN_ERR_TIMEOUT; the context stays usable."""
+    import exact_tiled_attention_16_gb300 as pkg
+    assert pkg.set_wait_timeout_ns(2_000_000) == 0  # 2 ms
+    try:
+        assert pkg.selftest_wait_timeout() == -8
+    finally:
+        assert pkg.set_wait_timeout_ns(4_000_000_000) == 0
+    assert pkg.check_device_errors()[0] == 0
+    w = synth.make_bf16(1, 1, 256, 64, False, seed=71)
+    o, lse = run_bf16(w)
+    assert_bf16_tol(compare_rows(w, o, lse), "after selftest")
+
+
+def test_torch_streams():
+    """The call is asynchronous on the given stream."""
+    import exact_tiled_attention_16_gb300 as pkg
+    w = synth.make_bf16(1, 2, 512, 128, False, seed=81)
+    q, k, v = to_device(w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = pkg.attn_fwd(q, k, v, scale=1 / math.sqrt(128))
+    s.synchronize()
+    assert_bf16_tol(compare_rows(w, o.float().cpu().numpy().astype(np.float64),
+                                 lse.cpu().numpy().astype(np.float64)), "side stream")
