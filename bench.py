@@ -1,0 +1,401 @@
+"""Benchmark of the exact attention forward pass on one GB300 (per process).
+
+One step = one call of the library's attention forward over the whole workload
+(all of the hot path: tile schedule, TMA loads, Q K^T, masked online softmax,
+P V, epilogue) with inputs resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3] [--impl ours|reference]
+
+Multi-GPU: the forward pass of independent problems has no exchange step, so
+N > 1 runs N independent replicas (one per rank, launched by torchrun); value is
+the work of all ranks divided by the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the only other implementation
+there is) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU-baseline leg uses numpy's BLAS; pin its thread count so the number of
+# cores it uses is known.
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_tiled_attention_16_gb300 import synth  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense BF16/FP8 tensor peak"
+L2_BYTES = 126 * 1024 * 1024
+KERNEL_SOURCES = ["exact_tiled_attention_16_gb300/csrc/attn_fwd_kernel.cuh",
+                  "exact_tiled_attention_16_gb300/csrc/ptx.cuh",
+                  "exact_tiled_attention_16_gb300/csrc/attn_api.cu"]
+WORKLOAD_TEXT = {
+    "cfg1": "bf16 B1 H2 N128 d64 non-causal",
+    "cfg2n": "bf16 B4 H16 N2048 d128 non-causal",
+    "cfg2c": "bf16 B4 H16 N2048 d128 causal",
+    "cfg3": "bf16 B1 H32 N16384 d128 causal (long sequence, small batch)",
+    "cfg4": "bf16 B16 H16 N4096 d64 non-causal, 2 shared Q/K outlier channels x20",
+    "cfg5": "e4m3 block-scaled B2 H16 N8192 d128 non-causal, rotated Q/K",
+}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def traffic_for(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm = float(f[1])
+                mx = float(f[2])
+            except ValueError:
+                continue
+            sms.append(sm)
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # samples taken while the GPU was loaded: the upper half of the clock samples
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 256, max_heads=None):
+    """Times the fp64 oracle on sampled rows of successive heads until budget_s
+    seconds of oracle time have passed; returns (TFLOP/s in the workload's
+    counting convention, sample description, seconds)."""
+    from oracle.attention import attention_head
+    flops = 0.0
+    elapsed = 0.0
+    heads = 0
+    rows_done = 0
+    for b in range(w.B):
+        for h in range(w.H):
+            q, k, v = w.head_f64(b, h)
+            rows = synth.sample_rows(w.N, rows_per_head, w.seed, b, h)
+            t0 = time.perf_counter()
+            attention_head(q, k, v, w.causal, w.scale, rows=rows)
+            elapsed += time.perf_counter() - t0
+            vis = (rows + 1) if w.causal else np.full(len(rows), w.N)
+            flops += float(4.0 * w.d * vis.sum())
+            heads += 1
+            rows_done += len(rows)
+            if elapsed >= budget_s or (max_heads and heads >= max_heads):
+                break
+        if elapsed >= budget_s or (max_heads and heads >= max_heads):
+            break
+    desc = (f"{rows_done} query rows ({rows_per_head} seeded rows per head x {heads} heads) against all "
+            f"visible keys of {w.name}; fp64 numpy, {_CORES} BLAS threads")
+    return flops / elapsed / 1e12, desc, elapsed
+
+
+def run_reference(args, world, rank):
+    """The oracle timed per step on a bounded sample (rank 0 only)."""
+    if rank != 0:
+        return
+    w = synth.make_config(args.workload) if not args.small else synth.make_bf16(1, 2, 1024, 128, True, 3)
+    from oracle.attention import attention_head
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    rows_per_step = 32
+
+    def step(i):
+        b, h = heads[i % len(heads)]
+        q, k, v = w.head_f64(b, h)
+        rows = synth.sample_rows(w.N, rows_per_step, w.seed + i, b, h)
+        t0 = time.perf_counter()
+        attention_head(q, k, v, w.causal, w.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        vis = (rows + 1) if w.causal else np.full(len(rows), w.N)
+        return dt, float(4.0 * w.d * vis.sum())
+
+    for i in range(args.warmup):
+        step(i)
+    tot_t = 0.0
+    tot_f = 0.0
+    for i in range(args.steps):
+        dt, f = step(args.warmup + i)
+        tot_t += dt
+        tot_f += f
+    value = tot_f / tot_t / 1e12
+    sample = (f"each step: {rows_per_step} seeded query rows of one head against all visible keys "
+              f"(fp64 numpy oracle, {_CORES} BLAS threads)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(args, w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(args, w):
+    in_bytes = w.q.nbytes + w.k.nbytes + w.v.nbytes
+    return {"workload": f"{w.name}: {WORKLOAD_TEXT.get(w.name, '')}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "causal": w.causal, "scale": w.scale, "seed": w.seed,
+            "l2": (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB); no flush"
+                   if in_bytes > L2_BYTES else
+                   "inputs smaller than L2: a 252 MiB buffer is written between steps; value from launch times"),
+            "parallelism": "replicas" if getattr(args, "gpus", 1) > 1 else "1 GPU"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cfg3", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true", help="(reference arm only) a small sample workload")
+    ap.add_argument("--custom", default=None,
+                    help="B,H,N,d,causal: a seeded bf16 workload of that shape instead of --workload "
+                         "(for profiling captures on a reduced case)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import exact_tiled_attention_16_gb300 as pkg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    if args.custom:
+        B, H, N, d, c = (int(x) for x in args.custom.split(","))
+        w = synth.make_bf16(B, H, N, d, bool(c), seed=3, name=f"custom_B{B}H{H}N{N}d{d}{'c' if c else 'n'}")
+    else:
+        w = synth.make_config(args.workload)
+    if w.dtype != "bf16":
+        raise SystemExit("the e4m3 workload is benchmarked through attn_fwd_fp8")
+    q_h, k_h, v_h = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+                     for x in (w.q, w.k, w.v))
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = w.flops()
+
+    in_bytes = q.nbytes + k.nbytes + v.nbytes
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if in_bytes <= L2_BYTES else None
+
+    def step():
+        if flush is not None:
+            flush.fill_(1.0)  # evicts the inputs from L2 (outside the kernel's own events)
+        pkg.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    rc, where = pkg.check_device_errors()
+    if rc != 0:
+        raise SystemExit(f"device error after warm-up (wait {where})")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_begin.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(1.0)
+            starts[i].record(stream)
+            pkg.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    rc, where = pkg.check_device_errors()
+    if rc != 0:
+        raise SystemExit(f"device error in the timed region (wait {where})")
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    avg_kernel_ms = sum(kern_ms) / len(kern_ms)
+    if flush is not None:
+        # the L2 flush between steps is not part of the step: time the launches only
+        t = torch.tensor([avg_kernel_ms], device=dev)
+        if pg:
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item()) * args.steps
+    ms_per_step = total_ms / args.steps
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, forward,
+    # O and LSE back to pinned host memory, every step.
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    qd, kd, vd = (torch.empty_like(q) for _ in range(3))
+
+    def e2e_step():
+        qd.copy_(q_h, non_blocking=True)
+        kd.copy_(k_h, non_blocking=True)
+        vd.copy_(v_h, non_blocking=True)
+        pkg.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": traffic_for(w.name),
+            "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3) from MEASURED_PEAKS.json"
+            if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16",
+            "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+            "kernel": "attn_fwd_bf16_kernel", "avg_launch_ms": avg_kernel_ms,
+            "flops_per_launch": flops}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs)",
+        "config": config_block(args, w),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
+                "h2d_bytes_per_step": int(q_h.nbytes + k_h.nbytes + v_h.nbytes),
+                "d2h_bytes_per_step": int(o_h.nbytes + l_h.nbytes)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, desc, secs = cpu_oracle_rate(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -148,8 +148,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.lse = lse;
   p.BH = BH;
   p.N = N;
-  p.num_qblocks = (N + kBlockM - 1) / kBlockM;
-  p.num_units = BH * p.num_qblocks;
+  p.num_kblocks = (N + kBlockN - 1) / kBlockN;
+  p.num_pairs = (N + kTilesPerUnit * kBlockM - 1) / (kTilesPerUnit * kBlockM);
+  p.num_units = BH * p.num_pairs;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;

@@ -10,21 +10,34 @@
 // page, "technical insight": running max and running normaliser with earlier
 // partial sums rescaled when a larger score arrives).
 //
-// Blackwell mapping of those ideas, one CTA per SM (persistent):
-//   warps 0-3  softmax: thread t owns query row t of the 128-row tile (TMEM lane t)
-//   warp  4    producer: TMA loads of Q once per tile and of K/V blocks into a
-//              ring of NSTAGE shared-memory stages
-//   warp  5    MMA issuer: S = Q K^T into TMEM (double-buffered), O += P V with P
-//              read from TMEM; also owns the TMEM allocation
-// TMEM columns: S buffers at 0 and 128 (fp32), O at 256 (D fp32 columns),
-// P at 384 (128 keys as bf16 pairs = 64 columns).
+// Blackwell mapping, one persistent CTA per SM.  A work unit is a pair of
+// 128-row query tiles (tile 0 = rows 256p..256p+127, tile 1 = the next 128) of one
+// (batch, head); both tiles stream the same K/V blocks:
+//   warps 0-3   softmax of tile 0 (thread t owns row t = TMEM lane t)
+//   warps 4-7   softmax of tile 1
+//   warp  8     producer: TMA loads of the two Q tiles and of the K/V blocks
+//               into a ring of NSTAGE shared-memory stages
+//   warp  9     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//   warps 10-11 idle (they give their registers to the softmax warps)
+// The MMA warp interleaves the tiles -- P0 V_j, S0 = Q0 K_{j+1}^T, P1 V_j,
+// S1 = Q1 K_{j+1}^T -- so that the softmax of one tile runs while the tensor
+// core works on the other.
 //
-// Work unit = (b*H + h, 128-row query block).  Units are handed out statically:
-// unit u of the run order goes to CTA (u mod G) on even rounds and to the mirror
-// CTA on odd rounds, so heavy and light causal units interleave across CTAs.
-// The run order is head-major so that concurrently running units share K/V in L2,
-// and under the causal mask each head's query blocks run from the heaviest (last)
-// to the lightest.
+// TMEM (512 columns x 128 lanes of 32 bit):  S_0 at 0, S_1 at 128 (fp32 scores),
+// O_0 at 256, O_1 at 256 + D (fp32 accumulators).  P_t (bf16, two per column)
+// overwrites the first 64 columns of S_t once the scores are in registers; the
+// next S_t = Q_t K^T is issued after O_t += P_t V, and tcgen05.mma operations
+// issued by one thread execute in issue order, so P_t is consumed before S_t is
+// rewritten.
+//
+// Synchronisation per tile t and K/V block j (all mbarriers):
+//   k_full/v_full[stage]  TMA -> MMA          kv_empty[stage]  MMA -> TMA
+//   s_full[t]   MMA -> softmax: S_t,j ready; since it is committed after
+//               O_t += P_t,j-1 V_j-1, it also means O_t and P_t are free
+//   p_full[t]   softmax -> MMA: P_t,j written (and O_t rescaled if needed)
+//   pv_done[t]  MMA -> softmax: the unit's last P_t V product has completed
+//   o_free[t]   softmax -> MMA: the epilogue has read O_t
+//   q_full/q_empty  Q tiles of a unit
 #pragma once
 
 #include <cuda.h>
@@ -35,14 +48,19 @@
 
 namespace attn {
 
-constexpr int kBlockM = 128;     // query rows per tile (= TMEM lanes)
-constexpr int kBlockN = 128;     // keys per K/V block
-constexpr int kNumThreads = 192; // 6 warps
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kBlockM = 128;      // query rows per tile (= TMEM lanes)
+constexpr int kBlockN = 128;      // keys per K/V block
+constexpr int kTilesPerUnit = 2;  // query tiles sharing the K/V stream
+constexpr int kNumThreads = 384;  // 12 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemP = 384;
+// Register split (setmaxnreg): the launch gives 168 registers per thread
+// (65536 / 384 rounded down to a multiple of 8); the two softmax warpgroups take
+// 216 and the control warpgroup keeps 72:  2*128*216 + 128*72 = 168*384.
+constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 216, kRegsControl = 72;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kRegsLaunch * kNumThreads,
+              "register split must add up to the launch allocation");
 // The running max is only moved when a block raises it by more than this many
 // powers of two; until then exponentials are taken against the stale max and are
 // at most 2^kRescaleThreshold, which bf16 P and the fp32 accumulators absorb.
@@ -53,8 +71,9 @@ struct FwdParams {
   float* lse;         // [B*H, N] or nullptr
   int BH;             // B*H
   int N;
-  int num_qblocks;    // ceil(N / 128)
-  int num_units;      // BH * num_qblocks
+  int num_kblocks;    // ceil(N / 128)
+  int num_pairs;      // ceil(N / 256): units per (b, h)
+  int num_units;      // BH * num_pairs
   int causal;
   float scale_log2;   // scale * log2(e)
   unsigned long long timeout_ns;
@@ -63,18 +82,29 @@ struct FwdParams {
 
 template <int D>
 struct SmemLayout {
-  static constexpr uint32_t kChunkBytes = kBlockM * 128;            // 128 rows x 128 bytes
-  static constexpr uint32_t kChunks = D / 64;                       // 64 bf16 per 128-byte row
-  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;     // one 128 x D bf16 tile
+  static constexpr uint32_t kChunkBytes = kBlockM * 128;         // 128 rows x 128 bytes
+  static constexpr uint32_t kChunks = D / 64;                    // 64 bf16 per 128-byte row
+  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;  // one 128 x D bf16 tile
 };
 
-__device__ __forceinline__ void unit_coords(int u, int num_qblocks, int causal, int& bh, int& qb) {
-  bh = u / num_qblocks;
-  const int r = u - bh * num_qblocks;
-  qb = causal ? (num_qblocks - 1 - r) : r;
+template <int D, int NSTAGE>
+constexpr size_t fwd_smem_bytes() {
+  return 1024 /*alignment slack*/ + SmemLayout<D>::kTileBytes * (kTilesPerUnit + 2 * NSTAGE) +
+         8 * (16 + 3 * NSTAGE) + 16;
 }
 
-// The unit index processed by this CTA in its `round`-th iteration (or -1).
+// Run order: head-major (units of one head are adjacent, so concurrently running
+// units share K/V in L2); under the causal mask each head's pairs run from the
+// heaviest (last rows) to the lightest.
+__device__ __forceinline__ void unit_coords(int u, int num_pairs, int causal, int& bh, int& pair) {
+  bh = u / num_pairs;
+  const int r = u - bh * num_pairs;
+  pair = causal ? (num_pairs - 1 - r) : r;
+}
+
+// The unit processed by this CTA in its `round`-th iteration (or -1): position
+// c of each round on even rounds, the mirror position on odd rounds, so that
+// heavy and light causal units interleave across CTAs.
 __device__ __forceinline__ int unit_for_round(int round, int num_units) {
   const int G = gridDim.x;
   const int c = blockIdx.x;
@@ -82,11 +112,11 @@ __device__ __forceinline__ int unit_for_round(int round, int num_units) {
   return pos < num_units ? pos : -1;
 }
 
-__device__ __forceinline__ int num_kv_blocks(int qb, int N, int causal) {
-  const int all = (N + kBlockN - 1) / kBlockN;
-  if (!causal) return all;
-  const int lim = qb + 1;  // kBlockM == kBlockN: keys up to the tile's last row
-  return lim < all ? lim : all;
+// K/V blocks that query tile `qt` (128-row block index) needs.
+__device__ __forceinline__ int num_kv_blocks(int qt, const FwdParams& p) {
+  if (!p.causal) return p.num_kblocks;
+  const int lim = qt + 1;  // kBlockM == kBlockN: keys up to the tile's last row
+  return lim < p.num_kblocks ? lim : p.num_kblocks;
 }
 
 // A wait taken by all 32 lanes of a warp that returns the same answer on every
@@ -97,35 +127,45 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <int D, int NSTAGE>
 __global__ void __launch_bounds__(kNumThreads, 1)
 attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
   using L = SmemLayout<D>;
+  constexpr uint32_t kTmemS[2] = {0, 128};
+  constexpr uint32_t kTmemO[2] = {256, 256 + D};
+
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms.
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
 
-  const uint32_t sQ = base;
-  const uint32_t sK = sQ + L::kTileBytes;
+  const uint32_t sQ = base;  // tile t at sQ + t * kTileBytes
+  const uint32_t sK = sQ + kTilesPerUnit * L::kTileBytes;
   const uint32_t sV = sK + NSTAGE * L::kTileBytes;
-  uint8_t* ctrl = smem + L::kTileBytes * (1 + 2 * NSTAGE);
-  // barriers (8 bytes each)
+  uint8_t* ctrl = smem + L::kTileBytes * (kTilesPerUnit + 2 * NSTAGE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(ctrl);
   const uint32_t b_q_full = smem_u32(&bars[0]);
   const uint32_t b_q_empty = smem_u32(&bars[1]);
-  const uint32_t b_pv_done = smem_u32(&bars[2]);
-  const uint32_t b_p_full = smem_u32(&bars[3]);
-  const uint32_t b_o_free = smem_u32(&bars[4]);
-  const uint32_t b_s_full0 = smem_u32(&bars[5]);   // +8*b for buffer b
-  const uint32_t b_s_free0 = smem_u32(&bars[7]);
-  const uint32_t b_drain = smem_u32(&bars[9]);
-  const uint32_t b_k_full0 = smem_u32(&bars[10]);  // +8*stage
-  const uint32_t b_v_full0 = smem_u32(&bars[10 + NSTAGE]);
-  const uint32_t b_kv_empty0 = smem_u32(&bars[10 + 2 * NSTAGE]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (10 + 3 * NSTAGE));
+  const uint32_t b_drain = smem_u32(&bars[2]);
+  const uint32_t b_s_full = smem_u32(&bars[4]);    // + 8 t
+  const uint32_t b_p_full = smem_u32(&bars[6]);    // + 8 t
+  const uint32_t b_pv_done = smem_u32(&bars[8]);   // + 8 t
+  const uint32_t b_o_free = smem_u32(&bars[10]);   // + 8 t
+  const uint32_t b_k_full = smem_u32(&bars[16]);   // + 8 stage
+  const uint32_t b_v_full = smem_u32(&bars[16 + NSTAGE]);
+  const uint32_t b_kv_empty = smem_u32(&bars[16 + 2 * NSTAGE]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (16 + 3 * NSTAGE));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -135,18 +175,17 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   if (threadIdx.x == 0) {
     mbar_init(b_q_full, 1);
     mbar_init(b_q_empty, 1);
-    mbar_init(b_pv_done, 1);
-    mbar_init(b_p_full, kSoftmaxWarps * 32);
-    mbar_init(b_o_free, kSoftmaxWarps * 32);
-    mbar_init(b_s_full0, 1);
-    mbar_init(b_s_full0 + 8, 1);
-    mbar_init(b_s_free0, kSoftmaxWarps * 32);
-    mbar_init(b_s_free0 + 8, kSoftmaxWarps * 32);
     mbar_init(b_drain, 1);
+    for (int t = 0; t < kTilesPerUnit; ++t) {
+      mbar_init(b_s_full + 8 * t, 1);
+      mbar_init(b_p_full + 8 * t, 128);
+      mbar_init(b_pv_done + 8 * t, 1);
+      mbar_init(b_o_free + 8 * t, 128);
+    }
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(b_k_full0 + 8 * s, 1);
-      mbar_init(b_v_full0 + 8 * s, 1);
-      mbar_init(b_kv_empty0 + 8 * s, 1);
+      mbar_init(b_k_full + 8 * s, 1);
+      mbar_init(b_v_full + 8 * s, 1);
+      mbar_init(b_kv_empty + 8 * s, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -165,156 +204,170 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ TMA
-    if (lane == 0) {
+  if (warp >= 8) {
+    setmaxnreg_dec<kRegsControl>();
+    if (warp == kProducerWarp && lane == 0) {
+      // ---------------------------------------------------------------- TMA
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       uint32_t kv_iter = 0;
-      int tiles = 0;
+      int units = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int u = unit_for_round(round, p.num_units);
         if (u < 0) break;
-        int bh, qb;
-        unit_coords(u, p.num_qblocks, p.causal, bh, qb);
-        const int nkv = num_kv_blocks(qb, p.N, p.causal);
-        if (tiles > 0 && !(ok = mbar_wait(b_q_empty, (tiles - 1) & 1, abort_flag, tmo, p.err, 1))) break;
-        mbar_arrive_expect_tx(b_q_full, L::kTileBytes);
-        for (int c = 0; c < (int)L::kChunks; ++c)
-          tma_load_3d(sQ + c * L::kChunkBytes, &tmap_q, b_q_full, c * 64, qb * kBlockM, bh, pol_q);
+        int bh, pair;
+        unit_coords(u, p.num_pairs, p.causal, bh, pair);
+        const int nkv = num_kv_blocks(2 * pair + 1, p);
+        if (units > 0 && !(ok = mbar_wait(b_q_empty, (units - 1) & 1, abort_flag, tmo, p.err, 1))) break;
+        mbar_arrive_expect_tx(b_q_full, kTilesPerUnit * L::kTileBytes);
+        for (int t = 0; t < kTilesPerUnit; ++t)
+          for (int c = 0; c < (int)L::kChunks; ++c)
+            tma_load_3d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tmap_q, b_q_full, c * 64,
+                        (2 * pair + t) * kBlockM, bh, pol_q);
         for (int j = 0; j < nkv; ++j, ++kv_iter) {
           const uint32_t st = kv_iter % NSTAGE;
           const uint32_t use = kv_iter / NSTAGE;
-          if (use > 0 && !(ok = mbar_wait(b_kv_empty0 + 8 * st, (use - 1) & 1, abort_flag, tmo, p.err, 2)))
+          if (use > 0 && !(ok = mbar_wait(b_kv_empty + 8 * st, (use - 1) & 1, abort_flag, tmo, p.err, 2)))
             break;
-          mbar_arrive_expect_tx(b_k_full0 + 8 * st, L::kTileBytes);
+          mbar_arrive_expect_tx(b_k_full + 8 * st, L::kTileBytes);
           for (int c = 0; c < (int)L::kChunks; ++c)
-            tma_load_3d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tmap_k, b_k_full0 + 8 * st, c * 64,
+            tma_load_3d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tmap_k, b_k_full + 8 * st, c * 64,
                         j * kBlockN, bh, pol_kv);
-          mbar_arrive_expect_tx(b_v_full0 + 8 * st, L::kTileBytes);
+          mbar_arrive_expect_tx(b_v_full + 8 * st, L::kTileBytes);
           for (int c = 0; c < (int)L::kChunks; ++c)
-            tma_load_3d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tmap_v, b_v_full0 + 8 * st, c * 64,
+            tma_load_3d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tmap_v, b_v_full + 8 * st, c * 64,
                         j * kBlockN, bh, pol_kv);
         }
-        ++tiles;
+        ++units;
       }
       // Tail: every copy issued has landed and every MMA commit that frees a
       // stage has arrived before the CTA may exit.  Waits are bounded.
+      const uint32_t first = kv_iter > NSTAGE ? kv_iter - NSTAGE : 0;
       if (ok) {
-        for (uint32_t i = (kv_iter > NSTAGE ? kv_iter - NSTAGE : 0); i < kv_iter; ++i) {
-          const uint32_t st = i % NSTAGE, use = i / NSTAGE;
-          mbar_wait(b_kv_empty0 + 8 * st, use & 1, abort_flag, tmo, p.err, 3);
-        }
-        if (tiles > 0) mbar_wait(b_q_empty, (tiles - 1) & 1, abort_flag, tmo, p.err, 4);
+        for (uint32_t i = first; i < kv_iter; ++i)
+          mbar_wait(b_kv_empty + 8 * (i % NSTAGE), (i / NSTAGE) & 1, abort_flag, tmo, p.err, 3);
+        if (units > 0) mbar_wait(b_q_empty, (units - 1) & 1, abort_flag, tmo, p.err, 4);
       } else {
-        // Error path: wait (bounded, ignoring the abort flag) for our own copies.
-        volatile int no_abort = 0;
-        for (uint32_t i = (kv_iter > NSTAGE ? kv_iter - NSTAGE : 0); i < kv_iter; ++i) {
-          const uint32_t st = i % NSTAGE, use = i / NSTAGE;
-          mbar_wait(b_k_full0 + 8 * st, use & 1, &no_abort, tmo, nullptr, 0);
-          mbar_wait(b_v_full0 + 8 * st, use & 1, &no_abort, tmo, nullptr, 0);
+        volatile int no_abort = 0;  // wait for our own copies even while aborting
+        for (uint32_t i = first; i < kv_iter; ++i) {
+          mbar_wait(b_k_full + 8 * (i % NSTAGE), (i / NSTAGE) & 1, &no_abort, tmo, nullptr, 0);
+          mbar_wait(b_v_full + 8 * (i % NSTAGE), (i / NSTAGE) & 1, &no_abort, tmo, nullptr, 0);
         }
-        if (tiles > 0) mbar_wait(b_q_full, (tiles - 1) & 1, &no_abort, tmo, nullptr, 0);
+        if (units > 0) mbar_wait(b_q_full, (units - 1) & 1, &no_abort, tmo, nullptr, 0);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
+      // ---------------------------------------------------------------- MMA
       constexpr uint32_t idesc_s = make_idesc(kBlockM, kBlockN, 1, false);
       constexpr uint32_t idesc_o = make_idesc(kBlockM, D, 1, true);
-      uint32_t kv_iter = 0, s_iter = 0, p_iter = 0;
-      int tiles = 0;
+      uint32_t kv_iter = 0;
+      uint32_t p_iter[2] = {0, 0};
+      int units = 0;
       bool ok = true;
+      // S_t = Q_t K^T for the K block in stage st
+      auto issue_s = [&](int t, uint32_t st) {
+        const uint32_t d_tmem = tmem + kTmemS[t];
+        const uint32_t q_base = sQ + t * L::kTileBytes;
+        const uint32_t k_base = sK + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          mma_f16_ss(d_tmem, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idesc_s,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit(b_s_full + 8 * t);
+      };
+      // O_t (+)= P_t V for the V block in stage st
+      auto issue_pv = [&](int t, uint32_t st, bool accumulate) {
+        const uint32_t v_base = sV + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_f16_ts(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8,
+                     sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), idesc_o,
+                     (accumulate || kk > 0) ? 1u : 0u);
+      };
       for (int round = 0; ok; ++round) {
         const int u = unit_for_round(round, p.num_units);
         if (u < 0) break;
-        int bh, qb;
-        unit_coords(u, p.num_qblocks, p.causal, bh, qb);
-        const int nkv = num_kv_blocks(qb, p.N, p.causal);
-        if (!(ok = mbar_wait(b_q_full, tiles & 1, abort_flag, tmo, p.err, 10))) break;
-        uint32_t prev_st = 0, prev_use = 0;
-        for (int j = 0; j <= nkv && ok; ++j) {
-          uint32_t st = 0, use = 0;
-          if (j < nkv) {
-            // S_j = Q K_j^T into S buffer (s_iter & 1)
-            st = kv_iter % NSTAGE;
-            use = kv_iter / NSTAGE;
-            const uint32_t b = s_iter & 1;
-            if (!(ok = mbar_wait(b_k_full0 + 8 * st, use & 1, abort_flag, tmo, p.err, 11))) break;
-            if (s_iter >= 2 && !(ok = mbar_wait(b_s_free0 + 8 * b, ((s_iter >> 1) - 1) & 1, abort_flag, tmo, p.err, 12)))
-              break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem + (b ? kTmemS1 : kTmemS0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-              mma_f16_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024),
-                         sdesc_sw128(sK + st * L::kTileBytes + off, 16, 1024), idesc_s, kk > 0);
-            }
-            mma_commit(b_s_full0 + 8 * b);
-            if (j == nkv - 1) mma_commit(b_q_empty);
-            ++s_iter;
-            ++kv_iter;
-          }
-          if (j >= 1) {
-            // O += P_{j-1} V_{j-1}
-            if (!(ok = mbar_wait(b_p_full, p_iter & 1, abort_flag, tmo, p.err, 13))) break;
-            ++p_iter;
-            if (!(ok = mbar_wait(b_v_full0 + 8 * prev_st, prev_use & 1, abort_flag, tmo, p.err, 14))) break;
-            if (j == 1 && tiles > 0 && !(ok = mbar_wait(b_o_free, (tiles - 1) & 1, abort_flag, tmo, p.err, 15)))
-              break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk) {
-              mma_f16_ts(tmem + kTmemO, tmem + kTmemP + kk * 8,
-                         sdesc_sw128(sV + prev_st * L::kTileBytes + kk * 16 * 128, L::kChunkBytes, 1024), idesc_o,
-                         (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(b_pv_done);
-            mma_commit(b_kv_empty0 + 8 * prev_st);
-          }
-          prev_st = st;
-          prev_use = use;
+        int bh, pair;
+        unit_coords(u, p.num_pairs, p.causal, bh, pair);
+        const int n0 = num_kv_blocks(2 * pair, p);
+        const int n1 = num_kv_blocks(2 * pair + 1, p);
+        if (!(ok = mbar_wait(b_q_full, units & 1, abort_flag, tmo, p.err, 10))) break;
+        {
+          const uint32_t st = kv_iter % NSTAGE;
+          if (!(ok = mbar_wait(b_k_full + 8 * st, (kv_iter / NSTAGE) & 1, abort_flag, tmo, p.err, 11))) break;
+          tc_fence_after();
+          issue_s(0, st);
+          issue_s(1, st);
+          if (n1 == 1) mma_commit(b_q_empty);
         }
-        ++tiles;
+        for (int j = 0; j < n1 && ok; ++j) {
+          const uint32_t it = kv_iter + j;
+          const uint32_t st = it % NSTAGE, ph = (it / NSTAGE) & 1;
+          const uint32_t stn = (it + 1) % NSTAGE, phn = ((it + 1) / NSTAGE) & 1;
+          for (int t = 0; t < kTilesPerUnit; ++t) {
+            const int nt = t == 0 ? n0 : n1;
+            if (j >= nt) continue;
+            if (!(ok = mbar_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
+            ++p_iter[t];
+            if (!(ok = mbar_wait(b_v_full + 8 * st, ph, abort_flag, tmo, p.err, 14))) break;
+            if (j == 0 && units > 0 &&
+                !(ok = mbar_wait(b_o_free + 8 * t, (units - 1) & 1, abort_flag, tmo, p.err, 15 + t)))
+              break;
+            tc_fence_after();
+            issue_pv(t, st, j > 0);
+            if (j == nt - 1) mma_commit(b_pv_done + 8 * t);
+            if (t == 1) mma_commit(b_kv_empty + 8 * st);
+            if (j + 1 < nt) {
+              if (!(ok = mbar_wait(b_k_full + 8 * stn, phn, abort_flag, tmo, p.err, 17))) break;
+              tc_fence_after();
+              issue_s(t, stn);
+              if (t == 1 && j + 1 == n1 - 1) mma_commit(b_q_empty);
+            }
+          }
+        }
+        kv_iter += n1;
+        ++units;
       }
-      // Make sure every MMA issued has completed before TMEM is released.
+      // Every MMA issued has completed before TMEM is released.
       mma_commit(b_drain);
       volatile int no_abort = 0;
       mbar_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
     }
   } else {
     // -------------------------------------------------------------- softmax
-    const int row_in_tile = threadIdx.x;  // 0..127, = TMEM lane
+    setmaxnreg_inc<kRegsSoftmax>();
+    const int t = warp >> 2;                      // query tile of this warpgroup
+    const int row_in_tile = threadIdx.x & 127;    // = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + kTmemS[t];
+    const uint32_t tO = tmem + lane_addr + kTmemO[t];
     const float sl2 = p.scale_log2;
     uint32_t s_iter = 0, pv_iter = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int u = unit_for_round(round, p.num_units);
       if (u < 0) break;
-      int bh, qb;
-      unit_coords(u, p.num_qblocks, p.causal, bh, qb);
-      const int nkv = num_kv_blocks(qb, p.N, p.causal);
-      const int row = qb * kBlockM + row_in_tile;
+      int bh, pair;
+      unit_coords(u, p.num_pairs, p.causal, bh, pair);
+      const int qt = 2 * pair + t;
+      const int nkv = num_kv_blocks(qt, p);
+      const int row = qt * kBlockM + row_in_tile;
       float m_use = -INFINITY;  // running max in log2 units (scale folded in)
       float l = 0.f;            // running normaliser against m_use
       for (int j = 0; j < nkv; ++j) {
-        const uint32_t b = s_iter & 1;
-        if (!(ok = warp_wait(b_s_full0 + 8 * b, (s_iter >> 1) & 1, abort_flag, tmo, p.err, 20))) break;
+        if (!(ok = warp_wait(b_s_full + 8 * t, s_iter & 1, abort_flag, tmo, p.err, 20 + t))) break;
+        ++s_iter;
         tc_fence_after();
         uint32_t sraw[kBlockN];
-        tmem_ld128_wait(tmem + lane_addr + (b ? kTmemS1 : kTmemS0), sraw);
-        tc_fence_before();
-        mbar_arrive(b_s_free0 + 8 * b);
-        ++s_iter;
+        tmem_ld128_wait(tS, sraw);
         float s[kBlockN];
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sraw[c]);
         // mask: causal (key > row) on the diagonal block, keys >= N on the tail block
         const int key0 = j * kBlockN;
-        if ((p.causal && j == qb) || key0 + kBlockN > p.N) {
+        if ((p.causal && j == qt) || key0 + kBlockN > p.N) {
           const int lim_causal = p.causal ? (row - key0) : (kBlockN - 1);
           const int lim_tail = p.N - 1 - key0;
           const int lim = lim_causal < lim_tail ? lim_causal : lim_tail;
@@ -322,10 +375,16 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           for (int c = 0; c < kBlockN; ++c)
             if (c > lim) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // row max: four independent chains of three-input max
+        float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
 #pragma unroll
-        for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
-        const float m_blk = mx * sl2;
+        for (int c = 4; c < kBlockN; c += 8) {
+          a0 = fmax3(a0, s[c], s[c + 1]);
+          a1 = fmax3(a1, s[c + 2], s[c + 3]);
+          a2 = fmax3(a2, s[c + 4], s[c + 5]);
+          a3 = fmax3(a3, s[c + 6], s[c + 7]);
+        }
+        const float m_blk = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
         float alpha = 1.f;
         bool moved = false;
         if (m_blk > m_use + kRescaleThreshold) {
@@ -333,49 +392,49 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           m_use = m_blk;
           moved = true;
         }
+        if (j > 0 && __any_sync(0xffffffffu, moved)) {
+          // O_t row *= alpha (alpha = 1 for rows whose max did not move).  The
+          // previous P_t V product has completed: s_full was committed after it.
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32_wait(tO + c0, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tO + c0, o);
+          }
+        }
         const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-        float rs = 0.f;
+        // P = 2^(s * scale*log2e - m), summed in four independent pairs of lanes
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
         uint32_t pk[kBlockN / 2];
 #pragma unroll
         for (int c = 0; c < kBlockN; c += 2) {
-          const float e0 = ex2_approx(fmaf(s[c], sl2, -m_sub));
-          const float e1 = ex2_approx(fmaf(s[c + 1], sl2, -m_sub));
-          rs += e0 + e1;
-          pk[c / 2] = pack_bf16x2(e0, e1);
+          const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(sl2, sl2), make_float2(-m_sub, -m_sub));
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
+          pk[c / 2] = pack_bf16x2(e.x, e.y);
         }
-        l = l * alpha + rs;
-        if (j >= 1) {
-          // P and O are still in use by the previous P V product.
-          if (!(ok = warp_wait(b_pv_done, pv_iter & 1, abort_flag, tmo, p.err, 21))) break;
-          ++pv_iter;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, moved)) {
-            // O row *= alpha (alpha = 1 for rows whose max did not move)
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t o[32];
-              tmem_ld32_wait(tmem + lane_addr + kTmemO + c0, o);
-#pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              tmem_st32(tmem + lane_addr + kTmemO + c0, o);
-            }
-          }
-        }
-        tmem_st64(tmem + lane_addr + kTmemP, pk);
+        const float2 acc01 = fadd2(acc[0], acc[1]);
+        const float2 acc23 = fadd2(acc[2], acc[3]);
+        const float2 accs = fadd2(acc01, acc23);
+        l = l * alpha + (accs.x + accs.y);
+        tmem_st64(tS, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b_p_full);
+        mbar_arrive(b_p_full + 8 * t);
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (!(ok = warp_wait(b_pv_done, pv_iter & 1, abort_flag, tmo, p.err, 22))) break;
+      if (!(ok = warp_wait(b_pv_done + 8 * t, pv_iter & 1, abort_flag, tmo, p.err, 22 + t))) break;
       ++pv_iter;
       tc_fence_after();
       uint32_t oraw[D];
-      if constexpr (D == 128) tmem_ld128_wait(tmem + lane_addr + kTmemO, oraw);
-      else tmem_ld64_wait(tmem + lane_addr + kTmemO, oraw);
+      if constexpr (D == 128) tmem_ld128_wait(tO, oraw);
+      else tmem_ld64_wait(tO, oraw);
       tc_fence_before();
-      mbar_arrive(b_o_free);  // the next tile's first P V may overwrite O now
+      mbar_arrive(b_o_free + 8 * t);  // the next unit's first P V may overwrite O_t now
       const float inv_l = 1.f / l;
       if (row < p.N) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.N + row) * D);
@@ -402,11 +461,6 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-template <int D, int NSTAGE>
-constexpr size_t fwd_smem_bytes() {
-  return 1024 /*alignment slack*/ + SmemLayout<D>::kTileBytes * (1 + 2 * NSTAGE) + 8 * (10 + 3 * NSTAGE) + 16;
 }
 
 }  // namespace attn
