@@ -9,7 +9,7 @@ functions load the library on first use and raise if it is missing.
 """
 from __future__ import annotations
 
-__all__ = ["attn_fwd", "attn_fwd_raw", "attn_status_string", "load_library", "AttnError",
+__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_fp8", "attn_fwd_fp8_raw", "attn_status_string", "load_library", "AttnError",
            "check_device_errors", "set_wait_timeout_ns", "selftest_wait_timeout"]
 
 

@@ -38,6 +38,8 @@ def load_library():
     vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp]
     lib.attn_fwd.restype = ci
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
+    lib.attn_fwd_fp8.restype = ci
     lib.attn_status_string.argtypes = [ci]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_check_device_errors.argtypes = [vp, ctypes.POINTER(ci)]
@@ -96,6 +98,43 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, 
                       _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_fp8_raw(q8: int, k8: int, v8: int, q_scale: int, k_scale: int, v_scale: int, o: int, lse: int,
+                     B: int, H: int, N: int, d: int, causal: bool, scale: float, stream: int) -> int:
+    """Direct call of the block-scaled FP8 entry point with device pointers."""
+    return load_library().attn_fwd_fp8(q8 or None, k8 or None, v8 or None, q_scale or None, k_scale or None,
+                                       v_scale or None, o or None, lse or None, B, H, N, d,
+                                       1 if causal else 0, float(scale), stream or None)
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, scale: float | None = None,
+                 o=None, lse=None, want_lse: bool = True, stream=None):
+    """Block-scaled FP8 attention forward for torch CUDA tensors.
+
+    q8, k8, v8: e4m3 codes [B,H,N,d] (torch.uint8 or torch.float8_e4m3fn);
+    *_scale: float32 [B,H,ceil(N/128)].  Returns (o bf16 [B,H,N,d], lse)."""
+    import torch
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous CUDA e4m3 (1-byte) tensor [B,H,N,d]")
+    B, H, N, d = q8.shape
+    T = (N + 127) // 128
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, H, T):
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor [B,H,ceil(N/128)]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    rc = attn_fwd_fp8_raw(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
+                          v_scale.data_ptr(), o.data_ptr(), lse.data_ptr() if lse is not None else 0,
+                          B, H, N, d, causal, scale, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
     return o, lse
 
 

@@ -51,14 +51,17 @@ EncodeTiledFn get_encode() {
   return g_encode;
 }
 
-template <int D, int NSTAGE>
-cudaError_t configure_bf16() {
-  return cudaFuncSetAttribute(attn_fwd_bf16_kernel<D, NSTAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(fwd_smem_bytes<D, NSTAGE>()));
+template <int D, int NK, int NV, bool kFp8>
+cudaError_t configure_kernel() {
+  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(SmemPlan<D, NK, NV, kFp8>::kBytes));
 }
 
-constexpr int kStages64 = 4;
-constexpr int kStages128 = 2;
+// Ring depths (K stages, V stages) per instance; shared memory holds the two Q
+// tiles, the rings and, for FP8, two f16 copies of V.
+#define ATTN_BF16_D64 64, 4, 4, false     // 32 KB + 4 x 16 KB + 4 x 16 KB
+#define ATTN_BF16_D128 128, 2, 2, false   // 64 KB + 2 x 32 KB + 2 x 32 KB
+#define ATTN_FP8_D128 128, 3, 3, true     // 32 KB + 3 x 16 KB + 3 x 16 KB + 2 x 32 KB
 
 // Per-device set-up on first use: architecture check, SM count, kernel
 // attributes, address of the error word.  Returns ATTN_OK or an error status.
@@ -79,7 +82,8 @@ int device_setup(int* dev_out) {
       st.status = ATTN_ERR_ARCH;
       return;
     }
-    if (configure_bf16<64, kStages64>() != cudaSuccess || configure_bf16<128, kStages128>() != cudaSuccess ||
+    if (configure_kernel<ATTN_BF16_D64>() != cudaSuccess || configure_kernel<ATTN_BF16_D128>() != cudaSuccess ||
+        configure_kernel<ATTN_FP8_D128>() != cudaSuccess ||
         cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_ptr), g_attn_err) != cudaSuccess) {
       st.status = ATTN_ERR_CUDA;
       return;
@@ -125,6 +129,30 @@ int validate_common(const void* q, const void* k, const void* v, const void* o, 
   return ATTN_OK;
 }
 
+void fill_params(FwdParams& p, void* o, float* lse, int BH, int N, int causal, float scale, int dev) {
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = BH;
+  p.N = N;
+  p.num_kblocks = (N + kBlockN - 1) / kBlockN;
+  p.num_pairs = (N + kTilesPerUnit * kBlockM - 1) / (kTilesPerUnit * kBlockM);
+  p.num_units = BH * p.num_pairs;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_scale = p.k_scale = p.v_scale = nullptr;
+  p.timeout_ns = g_timeout_ns;
+  p.err = g_dev[dev].err_ptr;
+}
+
+template <int D, int NK, int NV, bool kFp8>
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p, int dev,
+           void* stream) {
+  const int grid = p.num_units < g_dev[dev].num_sms ? p.num_units : g_dev[dev].num_sms;
+  attn_fwd_kernel<D, NK, NV, kFp8><<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8>::kBytes,
+                                     static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
 }  // namespace
 
 extern "C" {
@@ -142,30 +170,35 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if ((rc = make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
   if ((rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
   if ((rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
-
   FwdParams p;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.BH = BH;
-  p.N = N;
-  p.num_kblocks = (N + kBlockN - 1) / kBlockN;
-  p.num_pairs = (N + kTilesPerUnit * kBlockM - 1) / (kTilesPerUnit * kBlockM);
-  p.num_units = BH * p.num_pairs;
-  p.causal = causal ? 1 : 0;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.timeout_ns = g_timeout_ns;
-  p.err = g_dev[dev].err_ptr;
+  fill_params(p, o, lse, BH, N, causal, scale, dev);
+  if (d == 64) return launch<ATTN_BF16_D64>(mq, mk, mv, p, dev, stream);
+  return launch<ATTN_BF16_D128>(mq, mk, mv, p, dev, stream);
+}
 
-  const int grid = p.num_units < g_dev[dev].num_sms ? p.num_units : g_dev[dev].num_sms;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d == 64) {
-    attn_fwd_bf16_kernel<64, kStages64>
-        <<<grid, kNumThreads, fwd_smem_bytes<64, kStages64>(), s>>>(mq, mk, mv, p);
-  } else {
-    attn_fwd_bf16_kernel<128, kStages128>
-        <<<grid, kNumThreads, fwd_smem_bytes<128, kStages128>(), s>>>(mq, mk, mv, p);
-  }
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                 const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                 void* stream) {
+  int rc = validate_common(q8, k8, v8, o, lse, B, H, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  if (!q_scale || !k_scale || !v_scale) return ATTN_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return ATTN_ERR_ALIGN;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
+  if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
+  if ((rc = make_map(&mv, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
+  FwdParams p;
+  fill_params(p, o, lse, BH, N, causal, scale, dev);
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  return launch<ATTN_FP8_D128>(mq, mk, mv, p, dev, stream);
 }
 
 const char* attn_status_string(int status) {

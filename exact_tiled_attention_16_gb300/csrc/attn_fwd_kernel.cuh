@@ -15,29 +15,42 @@
 // (batch, head); both tiles stream the same K/V blocks:
 //   warps 0-3   softmax of tile 0 (thread t owns row t = TMEM lane t)
 //   warps 4-7   softmax of tile 1
-//   warp  8     producer: TMA loads of the two Q tiles and of the K/V blocks
-//               into a ring of NSTAGE shared-memory stages
+//   warp  8     producer: TMA loads of the two Q tiles and of the K and V
+//               blocks into two rings of shared-memory stages
 //   warp  9     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
-//   warps 10-11 idle (they give their registers to the softmax warps)
+//   warps 10-11 FP8 only: convert each e4m3 V block to f16 in shared memory
 // The MMA warp interleaves the tiles -- P0 V_j, S0 = Q0 K_{j+1}^T, P1 V_j,
 // S1 = Q1 K_{j+1}^T -- so that the softmax of one tile runs while the tensor
 // core works on the other.
 //
 // TMEM (512 columns x 128 lanes of 32 bit):  S_0 at 0, S_1 at 128 (fp32 scores),
-// O_0 at 256, O_1 at 256 + D (fp32 accumulators).  P_t (bf16, two per column)
+// O_0 at 256, O_1 at 256 + D (fp32 accumulators).  P_t (16-bit, two per column)
 // overwrites the first 64 columns of S_t once the scores are in registers; the
 // next S_t = Q_t K^T is issued after O_t += P_t V, and tcgen05.mma operations
 // issued by one thread execute in issue order, so P_t is consumed before S_t is
 // rewritten.
 //
-// Synchronisation per tile t and K/V block j (all mbarriers):
-//   k_full/v_full[stage]  TMA -> MMA          kv_empty[stage]  MMA -> TMA
+// Synchronisation (mbarriers):
+//   q_full/q_empty        the two Q tiles of a unit (TMA -> MMA -> TMA)
+//   k_full/k_empty[st]    K ring (TMA -> MMA; freed after the last S using it)
+//   v_full/v_empty[st]    V ring (TMA -> MMA, or -> converter for FP8)
+//   c_full/c_empty[b]     FP8: f16 copy of V (converter -> MMA -> converter)
 //   s_full[t]   MMA -> softmax: S_t,j ready; since it is committed after
 //               O_t += P_t,j-1 V_j-1, it also means O_t and P_t are free
 //   p_full[t]   softmax -> MMA: P_t,j written (and O_t rescaled if needed)
 //   pv_done[t]  MMA -> softmax: the unit's last P_t V product has completed
 //   o_free[t]   softmax -> MMA: the epilogue has read O_t
-//   q_full/q_empty  Q tiles of a unit
+//
+// Block-scaled FP8 variant (kFp8): Q, K, V are e4m3 with one fp32 scale per
+// (batch, head, 128-token block) -- the block quantisation and FP8 tensor-core
+// path of the FlashAttention-3 notes in the news article, section 1.
+// S = Q8 K8^T runs as tcgen05.mma kind::f8f6f4 and the true score is
+// s_q * s_k[j] * S, so s_q * s_k[j] is folded into the exponent multiplier.
+// P V runs as kind::f16: the e4m3 V codes are converted exactly to f16 in shared
+// memory and P is rounded to f16 (an e4m3 P loses too much precision once V has
+// outlier channels).  The V block scale and a 2^6 pre-scale are folded into the
+// exponent offset, P' = 2^(x - m + 6 + log2(s_v[j] / max s_v)) <= 2^14, and at
+// the end O = O' * max s_v / (64 l).
 #pragma once
 
 #include <cuda.h>
@@ -54,6 +67,8 @@ constexpr int kTilesPerUnit = 2;  // query tiles sharing the K/V stream
 constexpr int kNumThreads = 384;  // 12 warps
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kConvertWarp0 = 10;  // warps 10-11
+constexpr int kConvertThreads = 64;
 constexpr uint32_t kTmemCols = 512;
 // Register split (setmaxnreg): the launch gives 168 registers per thread
 // (65536 / 384 rounded down to a multiple of 8); the two softmax warpgroups take
@@ -63,8 +78,9 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kRegsLaunch * kNumT
               "register split must add up to the launch allocation");
 // The running max is only moved when a block raises it by more than this many
 // powers of two; until then exponentials are taken against the stale max and are
-// at most 2^kRescaleThreshold, which bf16 P and the fp32 accumulators absorb.
+// at most 2^8, which the 16-bit P and the fp32 accumulators absorb.
 constexpr float kRescaleThreshold = 8.0f;
+constexpr float kFp8PScaleLog2 = 6.0f;
 
 struct FwdParams {
   __nv_bfloat16* o;   // [B*H, N, D]
@@ -76,22 +92,41 @@ struct FwdParams {
   int num_units;      // BH * num_pairs
   int causal;
   float scale_log2;   // scale * log2(e)
+  const float* q_scale;  // FP8 only: [B*H, num_kblocks] block scales
+  const float* k_scale;
+  const float* v_scale;
   unsigned long long timeout_ns;
   int* err;           // device error word (first failure wins)
 };
 
-template <int D>
-struct SmemLayout {
+// A 128-row tile of D elements is stored as D*elem/128 column chunks of
+// 128 rows x 128 bytes (the TMA box and the 128-byte swizzle atom width).
+template <int D, int kElemBytes>
+struct TileLayout {
+  static constexpr uint32_t kChunkElems = 128 / kElemBytes;      // elements per 128-byte row
   static constexpr uint32_t kChunkBytes = kBlockM * 128;         // 128 rows x 128 bytes
-  static constexpr uint32_t kChunks = D / 64;                    // 64 bf16 per 128-byte row
-  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;  // one 128 x D bf16 tile
+  static constexpr uint32_t kChunks = D / kChunkElems;
+  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;  // one 128 x D tile
+  static constexpr uint32_t kMmaK = 32 / kElemBytes;             // K of one tcgen05.mma (32 bytes)
+  static_assert(kChunks >= 1, "head dimension too small for the 128-byte swizzle");
 };
 
-template <int D, int NSTAGE>
-constexpr size_t fwd_smem_bytes() {
-  return 1024 /*alignment slack*/ + SmemLayout<D>::kTileBytes * (kTilesPerUnit + 2 * NSTAGE) +
-         8 * (16 + 3 * NSTAGE) + 16;
-}
+// Shared-memory plan of one instance: Q tiles, K ring, V ring and (FP8) the f16
+// copy of V, then the mbarriers.
+template <int D, int NK, int NV, bool kFp8>
+struct SmemPlan {
+  using In = TileLayout<D, kFp8 ? 1 : 2>;   // Q, K, V as loaded
+  using V16 = TileLayout<D, 2>;              // V operand of P V (bf16 or f16)
+  static constexpr int kNumConv = kFp8 ? 2 : 0;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + kTilesPerUnit * In::kTileBytes;
+  static constexpr uint32_t kV = kK + NK * In::kTileBytes;
+  static constexpr uint32_t kC = kV + NV * In::kTileBytes;
+  static constexpr uint32_t kBars = kC + kNumConv * V16::kTileBytes;
+  static constexpr int kNumBars = 12 + 2 * NK + 2 * NV + 2 * kNumConv;
+  static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBars + 8 * kNumBars + 16;
+  static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
+};
 
 // Run order: head-major (units of one head are adjacent, so concurrently running
 // units share K/V in L2); under the causal mask each head's pairs run from the
@@ -136,11 +171,13 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D, int NSTAGE>
+template <int D, int NK, int NV, bool kFp8>
 __global__ void __launch_bounds__(kNumThreads, 1)
-attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
-  using L = SmemLayout<D>;
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+  using Plan = SmemPlan<D, NK, NV, kFp8>;
+  using L = typename Plan::In;
+  using LV = typename Plan::V16;
   constexpr uint32_t kTmemS[2] = {0, 128};
   constexpr uint32_t kTmemO[2] = {256, 256 + D};
 
@@ -150,11 +187,11 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
 
-  const uint32_t sQ = base;  // tile t at sQ + t * kTileBytes
-  const uint32_t sK = sQ + kTilesPerUnit * L::kTileBytes;
-  const uint32_t sV = sK + NSTAGE * L::kTileBytes;
-  uint8_t* ctrl = smem + L::kTileBytes * (kTilesPerUnit + 2 * NSTAGE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ctrl);
+  const uint32_t sQ = base + Plan::kQ;  // tile t at sQ + t * kTileBytes
+  const uint32_t sK = base + Plan::kK;
+  const uint32_t sV = base + Plan::kV;
+  const uint32_t sC = base + Plan::kC;  // FP8: f16 V buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Plan::kBars);
   const uint32_t b_q_full = smem_u32(&bars[0]);
   const uint32_t b_q_empty = smem_u32(&bars[1]);
   const uint32_t b_drain = smem_u32(&bars[2]);
@@ -162,10 +199,13 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   const uint32_t b_p_full = smem_u32(&bars[6]);    // + 8 t
   const uint32_t b_pv_done = smem_u32(&bars[8]);   // + 8 t
   const uint32_t b_o_free = smem_u32(&bars[10]);   // + 8 t
-  const uint32_t b_k_full = smem_u32(&bars[16]);   // + 8 stage
-  const uint32_t b_v_full = smem_u32(&bars[16 + NSTAGE]);
-  const uint32_t b_kv_empty = smem_u32(&bars[16 + 2 * NSTAGE]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (16 + 3 * NSTAGE));
+  const uint32_t b_k_full = smem_u32(&bars[12]);   // + 8 stage
+  const uint32_t b_k_empty = smem_u32(&bars[12 + NK]);
+  const uint32_t b_v_full = smem_u32(&bars[12 + 2 * NK]);
+  const uint32_t b_v_empty = smem_u32(&bars[12 + 2 * NK + NV]);
+  const uint32_t b_c_full = smem_u32(&bars[12 + 2 * NK + 2 * NV]);  // + 8 b (FP8)
+  const uint32_t b_c_empty = b_c_full + 8 * Plan::kNumConv;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[Plan::kNumBars]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -182,10 +222,17 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       mbar_init(b_pv_done + 8 * t, 1);
       mbar_init(b_o_free + 8 * t, 128);
     }
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(b_k_full + 8 * s, 1);
+      mbar_init(b_k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(b_v_full + 8 * s, 1);
-      mbar_init(b_kv_empty + 8 * s, 1);
+      mbar_init(b_v_empty + 8 * s, kFp8 ? kConvertThreads : 1);
+    }
+    for (int b = 0; b < Plan::kNumConv; ++b) {
+      mbar_init(b_c_full + 8 * b, kConvertThreads);
+      mbar_init(b_c_empty + 8 * b, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -210,8 +257,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       // ---------------------------------------------------------------- TMA
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      uint32_t kv_iter = 0;
-      int units = 0;
+      uint32_t gk = 0, gv = 0;  // K and V blocks issued so far
+      int units = 0, q_issued = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int u = unit_for_round(round, p.num_units);
@@ -223,67 +270,78 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         mbar_arrive_expect_tx(b_q_full, kTilesPerUnit * L::kTileBytes);
         for (int t = 0; t < kTilesPerUnit; ++t)
           for (int c = 0; c < (int)L::kChunks; ++c)
-            tma_load_3d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tmap_q, b_q_full, c * 64,
+            tma_load_3d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tmap_q, b_q_full, c * L::kChunkElems,
                         (2 * pair + t) * kBlockM, bh, pol_q);
-        for (int j = 0; j < nkv; ++j, ++kv_iter) {
-          const uint32_t st = kv_iter % NSTAGE;
-          const uint32_t use = kv_iter / NSTAGE;
-          if (use > 0 && !(ok = mbar_wait(b_kv_empty + 8 * st, (use - 1) & 1, abort_flag, tmo, p.err, 2)))
-            break;
-          mbar_arrive_expect_tx(b_k_full + 8 * st, L::kTileBytes);
+        ++q_issued;
+        for (int j = 0; j < nkv; ++j) {
+          const uint32_t sk = gk % NK, uk = gk / NK;
+          if (uk > 0 && !(ok = mbar_wait(b_k_empty + 8 * sk, (uk - 1) & 1, abort_flag, tmo, p.err, 2))) break;
+          mbar_arrive_expect_tx(b_k_full + 8 * sk, L::kTileBytes);
           for (int c = 0; c < (int)L::kChunks; ++c)
-            tma_load_3d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tmap_k, b_k_full + 8 * st, c * 64,
-                        j * kBlockN, bh, pol_kv);
-          mbar_arrive_expect_tx(b_v_full + 8 * st, L::kTileBytes);
+            tma_load_3d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tmap_k, b_k_full + 8 * sk,
+                        c * L::kChunkElems, j * kBlockN, bh, pol_kv);
+          ++gk;
+          const uint32_t sv = gv % NV, uv = gv / NV;
+          if (uv > 0 && !(ok = mbar_wait(b_v_empty + 8 * sv, (uv - 1) & 1, abort_flag, tmo, p.err, 3))) break;
+          mbar_arrive_expect_tx(b_v_full + 8 * sv, L::kTileBytes);
           for (int c = 0; c < (int)L::kChunks; ++c)
-            tma_load_3d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tmap_v, b_v_full + 8 * st, c * 64,
-                        j * kBlockN, bh, pol_kv);
+            tma_load_3d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tmap_v, b_v_full + 8 * sv,
+                        c * L::kChunkElems, j * kBlockN, bh, pol_kv);
+          ++gv;
         }
         ++units;
       }
-      // Tail: every copy issued has landed and every MMA commit that frees a
-      // stage has arrived before the CTA may exit.  Waits are bounded.
-      const uint32_t first = kv_iter > NSTAGE ? kv_iter - NSTAGE : 0;
+      // Tail: every copy issued has landed and every consumer that frees a stage
+      // has arrived before the CTA may exit.  Waits are bounded.
       if (ok) {
-        for (uint32_t i = first; i < kv_iter; ++i)
-          mbar_wait(b_kv_empty + 8 * (i % NSTAGE), (i / NSTAGE) & 1, abort_flag, tmo, p.err, 3);
-        if (units > 0) mbar_wait(b_q_empty, (units - 1) & 1, abort_flag, tmo, p.err, 4);
+        for (uint32_t i = (gk > NK ? gk - NK : 0); i < gk; ++i)
+          mbar_wait(b_k_empty + 8 * (i % NK), (i / NK) & 1, abort_flag, tmo, p.err, 4);
+        for (uint32_t i = (gv > NV ? gv - NV : 0); i < gv; ++i)
+          mbar_wait(b_v_empty + 8 * (i % NV), (i / NV) & 1, abort_flag, tmo, p.err, 5);
+        if (units > 0) mbar_wait(b_q_empty, (units - 1) & 1, abort_flag, tmo, p.err, 6);
       } else {
-        volatile int no_abort = 0;  // wait for our own copies even while aborting
-        for (uint32_t i = first; i < kv_iter; ++i) {
-          mbar_wait(b_k_full + 8 * (i % NSTAGE), (i / NSTAGE) & 1, &no_abort, tmo, nullptr, 0);
-          mbar_wait(b_v_full + 8 * (i % NSTAGE), (i / NSTAGE) & 1, &no_abort, tmo, nullptr, 0);
-        }
-        if (units > 0) mbar_wait(b_q_full, (units - 1) & 1, &no_abort, tmo, nullptr, 0);
+        // Error path: wait (bounded, ignoring the abort flag) for our own copies.
+        volatile int no_abort = 0;
+        for (uint32_t i = (gk > NK ? gk - NK : 0); i < gk; ++i)
+          mbar_wait(b_k_full + 8 * (i % NK), (i / NK) & 1, &no_abort, tmo, nullptr, 0);
+        for (uint32_t i = (gv > NV ? gv - NV : 0); i < gv; ++i)
+          mbar_wait(b_v_full + 8 * (i % NV), (i / NV) & 1, &no_abort, tmo, nullptr, 0);
+        if (q_issued > 0) mbar_wait(b_q_full, (q_issued - 1) & 1, &no_abort, tmo, nullptr, 0);
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------------- MMA
-      constexpr uint32_t idesc_s = make_idesc(kBlockM, kBlockN, 1, false);
-      constexpr uint32_t idesc_o = make_idesc(kBlockM, D, 1, true);
-      uint32_t kv_iter = 0;
+      // S: bf16 (kind::f16, format 1) or e4m3 (kind::f8f6f4, format 0).
+      // P V: kind::f16 with bf16 (BF16 path) or f16 (FP8 path: format 0) operands.
+      constexpr uint32_t idesc_s = make_idesc(kBlockM, kBlockN, kFp8 ? 0u : 1u, false);
+      constexpr uint32_t idesc_o = make_idesc(kBlockM, D, kFp8 ? 0u : 1u, true);
+      uint32_t g = 0;
       uint32_t p_iter[2] = {0, 0};
       int units = 0;
       bool ok = true;
-      // S_t = Q_t K^T for the K block in stage st
-      auto issue_s = [&](int t, uint32_t st) {
+      // S_t = Q_t K^T for the K block in stage sk: K steps of 32 bytes, four per
+      // 128-byte swizzled row, then on to the next column chunk.
+      auto issue_s = [&](int t, uint32_t sk) {
         const uint32_t d_tmem = tmem + kTmemS[t];
         const uint32_t q_base = sQ + t * L::kTileBytes;
-        const uint32_t k_base = sK + st * L::kTileBytes;
+        const uint32_t k_base = sK + sk * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / (int)L::kMmaK; ++kk) {
           const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_f16_ss(d_tmem, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idesc_s,
-                     kk > 0 ? 1u : 0u);
+          const uint64_t da = sdesc_sw128(q_base + off, 16, 1024);
+          const uint64_t db = sdesc_sw128(k_base + off, 16, 1024);
+          if constexpr (kFp8) mma_f8_ss(d_tmem, da, db, idesc_s, kk > 0 ? 1u : 0u);
+          else mma_f16_ss(d_tmem, da, db, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(b_s_full + 8 * t);
       };
-      // O_t (+)= P_t V for the V block in stage st
-      auto issue_pv = [&](int t, uint32_t st, bool accumulate) {
-        const uint32_t v_base = sV + st * L::kTileBytes;
+      // O_t (+)= P_t V with the 16-bit V tile at v_base: P_t from TMEM (two keys
+      // per column), V MN-major, 16 key rows of 128 bytes per step, column chunks
+      // kChunkBytes apart.
+      auto issue_pv = [&](int t, uint32_t v_base, bool accumulate) {
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           mma_f16_ts(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8,
-                     sdesc_sw128(v_base + kk * 16 * 128, L::kChunkBytes, 1024), idesc_o,
+                     sdesc_sw128(v_base + kk * 16 * 128, LV::kChunkBytes, 1024), idesc_o,
                      (accumulate || kk > 0) ? 1u : 0u);
       };
       for (int round = 0; ok; ++round) {
@@ -295,45 +353,109 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         const int n1 = num_kv_blocks(2 * pair + 1, p);
         if (!(ok = mbar_wait(b_q_full, units & 1, abort_flag, tmo, p.err, 10))) break;
         {
-          const uint32_t st = kv_iter % NSTAGE;
-          if (!(ok = mbar_wait(b_k_full + 8 * st, (kv_iter / NSTAGE) & 1, abort_flag, tmo, p.err, 11))) break;
+          const uint32_t sk = g % NK;
+          if (!(ok = mbar_wait(b_k_full + 8 * sk, (g / NK) & 1, abort_flag, tmo, p.err, 11))) break;
           tc_fence_after();
-          issue_s(0, st);
-          issue_s(1, st);
+          issue_s(0, sk);
+          issue_s(1, sk);
+          mma_commit(b_k_empty + 8 * sk);
           if (n1 == 1) mma_commit(b_q_empty);
         }
         for (int j = 0; j < n1 && ok; ++j) {
-          const uint32_t it = kv_iter + j;
-          const uint32_t st = it % NSTAGE, ph = (it / NSTAGE) & 1;
-          const uint32_t stn = (it + 1) % NSTAGE, phn = ((it + 1) / NSTAGE) & 1;
+          const uint32_t gj = g + j;
+          const uint32_t skn = (gj + 1) % NK, phkn = ((gj + 1) / NK) & 1;
+          // the 16-bit V operand of block j
+          uint32_t v_base, v_bar, v_par;
+          if constexpr (kFp8) {
+            v_base = sC + (gj & 1) * LV::kTileBytes;
+            v_bar = b_c_full + 8 * (gj & 1);
+            v_par = (gj >> 1) & 1;
+          } else {
+            v_base = sV + (gj % NV) * L::kTileBytes;
+            v_bar = b_v_full + 8 * (gj % NV);
+            v_par = (gj / NV) & 1;
+          }
           for (int t = 0; t < kTilesPerUnit; ++t) {
             const int nt = t == 0 ? n0 : n1;
             if (j >= nt) continue;
             if (!(ok = mbar_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
             ++p_iter[t];
-            if (!(ok = mbar_wait(b_v_full + 8 * st, ph, abort_flag, tmo, p.err, 14))) break;
+            if (!(ok = mbar_wait(v_bar, v_par, abort_flag, tmo, p.err, 14))) break;
             if (j == 0 && units > 0 &&
                 !(ok = mbar_wait(b_o_free + 8 * t, (units - 1) & 1, abort_flag, tmo, p.err, 15 + t)))
               break;
             tc_fence_after();
-            issue_pv(t, st, j > 0);
+            issue_pv(t, v_base, j > 0);
             if (j == nt - 1) mma_commit(b_pv_done + 8 * t);
-            if (t == 1) mma_commit(b_kv_empty + 8 * st);
+            if (t == 1) {
+              // tile 1 is the last user of V_j
+              if constexpr (kFp8) mma_commit(b_c_empty + 8 * (gj & 1));
+              else mma_commit(b_v_empty + 8 * (gj % NV));
+            }
             if (j + 1 < nt) {
-              if (!(ok = mbar_wait(b_k_full + 8 * stn, phn, abort_flag, tmo, p.err, 17))) break;
+              if (!(ok = mbar_wait(b_k_full + 8 * skn, phkn, abort_flag, tmo, p.err, 17))) break;
               tc_fence_after();
-              issue_s(t, stn);
-              if (t == 1 && j + 1 == n1 - 1) mma_commit(b_q_empty);
+              issue_s(t, skn);
+              if (t == 1) {
+                mma_commit(b_k_empty + 8 * skn);  // tile 1 is the last user of K_{j+1}
+                if (j + 1 == n1 - 1) mma_commit(b_q_empty);
+              }
             }
           }
         }
-        kv_iter += n1;
+        g += n1;
         ++units;
       }
       // Every MMA issued has completed before TMEM is released.
       mma_commit(b_drain);
       volatile int no_abort = 0;
       mbar_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
+    } else if (kFp8 && warp >= kConvertWarp0) {
+      // ------------------------------------------------- FP8: V e4m3 -> f16
+      // Each thread converts 16 of the 1024 16-byte units of a V block (128 key
+      // rows x 128 e4m3): the 16 codes of a unit become 32 bytes of f16 in the
+      // MN-major, 128-byte-swizzled layout the P V MMA reads (two column chunks
+      // of 64 channels).  Codes are exact in f16.
+      const int ct = threadIdx.x - kConvertWarp0 * 32;  // 0..63
+      uint32_t g = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int u = unit_for_round(round, p.num_units);
+        if (u < 0) break;
+        int bh, pair;
+        unit_coords(u, p.num_pairs, p.causal, bh, pair);
+        const int nkv = num_kv_blocks(2 * pair + 1, p);
+        for (int j = 0; j < nkv && ok; ++j, ++g) {
+          const uint32_t sv = g % NV, b = g & 1;
+          if (!(ok = mbar_wait(b_v_full + 8 * sv, (g / NV) & 1, abort_flag, tmo, p.err, 30))) break;
+          if (g >= 2 && !(ok = mbar_wait(b_c_empty + 8 * b, ((g >> 1) - 1) & 1, abort_flag, tmo, p.err, 31)))
+            break;
+          const uint8_t* src = smem + Plan::kV + sv * L::kTileBytes;
+          uint8_t* dst = smem + Plan::kC + b * LV::kTileBytes;
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int idx = ct + kConvertThreads * it;  // 0..1023
+            const int r = idx >> 3;                     // key row
+            const int lu = idx & 7;                     // logical unit: channels 16 lu .. 16 lu + 15
+            const uint4 in = *reinterpret_cast<const uint4*>(src + r * 128 + ((lu ^ (r & 7)) << 4));
+            const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              h[2 * e] = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(w[e] & 0xffffu));
+              h[2 * e + 1] = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(w[e] >> 16));
+            }
+            const int chunk = lu >> 2;    // channels 0-63 / 64-127
+            const int x0 = (lu & 3) * 2;  // first 16-byte f16 unit of the pair
+            uint8_t* rowp = dst + chunk * LV::kChunkBytes + r * 128;
+            *reinterpret_cast<uint4*>(rowp + ((x0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(rowp + (((x0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+          mbar_arrive(b_c_full + 8 * b);
+          mbar_arrive(b_v_empty + 8 * sv);
+        }
+      }
     }
   } else {
     // -------------------------------------------------------------- softmax
@@ -343,7 +465,6 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + kTmemS[t];
     const uint32_t tO = tmem + lane_addr + kTmemO[t];
-    const float sl2 = p.scale_log2;
     uint32_t s_iter = 0, pv_iter = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -354,9 +475,28 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       const int qt = 2 * pair + t;
       const int nkv = num_kv_blocks(qt, p);
       const int row = qt * kBlockM + row_in_tile;
+      // Exponent multiplier of the raw scores (log2 units); FP8 adds s_q * s_k[j].
+      float c_q = p.scale_log2;
+      float sv_max = 1.f;
+      const float* ks_row = nullptr;
+      const float* vs_row = nullptr;
+      if constexpr (kFp8) {
+        const size_t sb = static_cast<size_t>(bh) * p.num_kblocks;
+        ks_row = p.k_scale + sb;
+        vs_row = p.v_scale + sb;
+        c_q *= __ldg(p.q_scale + sb + (qt < p.num_kblocks ? qt : p.num_kblocks - 1));
+        sv_max = 0.f;  // largest V block scale this tile uses (scales are > 0)
+        for (int jj = 0; jj < nkv; ++jj) sv_max = fmaxf(sv_max, __ldg(vs_row + jj));
+      }
       float m_use = -INFINITY;  // running max in log2 units (scale folded in)
       float l = 0.f;            // running normaliser against m_use
       for (int j = 0; j < nkv; ++j) {
+        float cj = c_q;
+        float off = 0.f;  // FP8: log2 of the pre-scale and V block-scale ratio
+        if constexpr (kFp8) {
+          cj *= __ldg(ks_row + j);
+          off = kFp8PScaleLog2 + lg2_approx(__ldg(vs_row + j) / sv_max);
+        }
         if (!(ok = warp_wait(b_s_full + 8 * t, s_iter & 1, abort_flag, tmo, p.err, 20 + t))) break;
         ++s_iter;
         tc_fence_after();
@@ -384,7 +524,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           a2 = fmax3(a2, s[c + 4], s[c + 5]);
           a3 = fmax3(a3, s[c + 6], s[c + 7]);
         }
-        const float m_blk = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
+        const float m_blk = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * cj;
         float alpha = 1.f;
         bool moved = false;
         if (m_blk > m_use + kRescaleThreshold) {
@@ -404,22 +544,25 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tmem_st32(tO + c0, o);
           }
         }
-        const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-        // P = 2^(s * scale*log2e - m), summed in four independent pairs of lanes
+        // P = 2^(s * cj - m [+ off]), summed in four independent pairs of lanes
+        const float m_sub = ((m_use == -INFINITY) ? 0.f : m_use) - off;
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         uint32_t pk[kBlockN / 2];
 #pragma unroll
         for (int c = 0; c < kBlockN; c += 2) {
-          const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(sl2, sl2), make_float2(-m_sub, -m_sub));
+          const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(cj, cj), make_float2(-m_sub, -m_sub));
           const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
-          pk[c / 2] = pack_bf16x2(e.x, e.y);
+          if constexpr (kFp8) pk[c / 2] = pack_f16x2(e.x, e.y);
+          else pk[c / 2] = pack_bf16x2(e.x, e.y);
         }
         const float2 acc01 = fadd2(acc[0], acc[1]);
         const float2 acc23 = fadd2(acc[2], acc[3]);
         const float2 accs = fadd2(acc01, acc23);
-        l = l * alpha + (accs.x + accs.y);
+        float rowsum = accs.x + accs.y;
+        if constexpr (kFp8) rowsum *= ex2_approx(-off);  // back to the unscaled P
+        l = l * alpha + rowsum;
         tmem_st64(tS, pk);
         tmem_st_wait();
         tc_fence_before();
@@ -435,7 +578,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       else tmem_ld64_wait(tO, oraw);
       tc_fence_before();
       mbar_arrive(b_o_free + 8 * t);  // the next unit's first P V may overwrite O_t now
-      const float inv_l = 1.f / l;
+      const float inv_l = (kFp8 ? sv_max * (1.f / 64.f) : 1.f) / l;
       if (row < p.N) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.N + row) * D);
 #pragma unroll

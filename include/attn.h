@@ -71,6 +71,24 @@ typedef enum { ATTN_BF16 = 0 } attn_dtype;
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              int causal, float scale, int dtype, void* stream);
 
+/*
+ * attn_fwd_fp8 -- block-scaled FP8 exact attention forward (FlashAttention-3's
+ * FP8 path with block quantisation, news article section 1).
+ *   q8, k8, v8 : const e4m3 codes (OCP FP8 E4M3) [B,H,N,d], 16-byte aligned
+ *   q_scale, k_scale, v_scale : const float32 [B,H,ceil(N/128)], 4-byte aligned,
+ *                finite and > 0: the value of element [b,h,n,c] is
+ *                decode(x8[b,h,n,c]) * x_scale[b,h,n/128]
+ *   o          : bf16 [B,H,N,d] output;  lse : float32 [B,H,N] or NULL
+ *   d          : 128 (other head dimensions return ATTN_ERR_UNSUPPORTED_HEADDIM)
+ *   other arguments as attn_fwd.
+ * Arithmetic: e4m3 Q K^T and P V on the tensor cores (fp32 accumulation), softmax
+ * in fp32 on the dequantised scores, P rounded to e4m3 (pre-scaled into e4m3's
+ * normal range), O rounded to bf16.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                 const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                 void* stream);
+
 /* Human-readable name of an attn_status value (static storage). */
 const char* attn_status_string(int status);
 

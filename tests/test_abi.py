@@ -76,6 +76,23 @@ def test_validation_codes(lib, kwargs, code):
     assert _call(lib, **kwargs) == code
 
 
+def _call_fp8(lib, d=128, qs=0x6000, **kw):
+    import exact_tiled_attention_16_gb300._lib as L
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=128, causal=0, scale=0.125)
+    args.update(kw)
+    return L.attn_fwd_fp8_raw(args["q"], args["k"], args["v"], qs, 0x7000, 0x8000, args["o"], args["lse"],
+                              args["B"], args["H"], args["N"], d, args["causal"], args["scale"], 0)
+
+
+def test_fp8_validation_codes(lib):
+    assert _call_fp8(lib, d=64) == -3
+    assert _call_fp8(lib, qs=0) == -1
+    assert _call_fp8(lib, qs=0x6002) == -5
+    assert _call_fp8(lib, q=0) == -1
+    assert _call_fp8(lib, N=0) == -2
+    assert _call_fp8(lib, scale=0.0) == -10
+
+
 def test_wait_timeout_setter(lib):
     assert lib.attn_set_wait_timeout_ns(10) == -2
     assert lib.attn_set_wait_timeout_ns(4_000_000_000) == 0
