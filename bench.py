@@ -140,6 +140,22 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """The largest of `value` across the ranks of the default process group (the
+    slowest rank's time); `dist` is torch.distributed or None for one process."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, world: int, steps: int, slowest_ms: float) -> float:
+    """TFLOP/s of the whole job: the work of all ranks over the slowest rank's time."""
+    return flops_per_step * world * steps / (slowest_ms * 1e-3) / 1e12
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -266,15 +282,26 @@ def main():
         w = synth.make_bf16(B, H, N, d, bool(c), seed=3, name=f"custom_B{B}H{H}N{N}d{d}{'c' if c else 'n'}")
     else:
         w = synth.make_config(args.workload)
-    if w.dtype != "bf16":
-        raise SystemExit("the e4m3 workload is benchmarked through attn_fwd_fp8")
-    q_h, k_h, v_h = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
-                     for x in (w.q, w.k, w.v))
+    fp8 = w.dtype == "e4m3"
+    if fp8:
+        q_h, k_h, v_h = (torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (w.q, w.k, w.v))
+        sc_h = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (w.q_scale, w.k_scale, w.v_scale)]
+        scales = [t.to(dev) for t in sc_h]
+    else:
+        q_h, k_h, v_h = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+                         for x in (w.q, w.k, w.v))
+        sc_h, scales = [], []
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    o = torch.empty_like(q)
+    o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     flops = w.flops()
+
+    def forward(qq, kk, vv, ss):
+        if fp8:
+            pkg.attn_fwd_fp8(qq, kk, vv, *ss, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        else:
+            pkg.attn_fwd(qq, kk, vv, causal=w.causal, scale=w.scale, o=o, lse=lse)
 
     in_bytes = q.nbytes + k.nbytes + v.nbytes
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if in_bytes <= L2_BYTES else None
@@ -282,7 +309,7 @@ def main():
     def step():
         if flush is not None:
             flush.fill_(1.0)  # evicts the inputs from L2 (outside the kernel's own events)
-        pkg.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        forward(q, k, v, scales)
 
     for _ in range(args.warmup):
         step()
@@ -304,7 +331,7 @@ def main():
             if flush is not None:
                 flush.fill_(1.0)
             starts[i].record(stream)
-            pkg.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+            forward(q, k, v, scales)
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
@@ -315,19 +342,13 @@ def main():
     rc, where = pkg.check_device_errors()
     if rc != 0:
         raise SystemExit(f"device error in the timed region (wait {where})")
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, total_ms, dev)
     avg_kernel_ms = sum(kern_ms) / len(kern_ms)
     if flush is not None:
         # the L2 flush between steps is not part of the step: time the launches only
-        t = torch.tensor([avg_kernel_ms], device=dev)
-        if pg:
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item()) * args.steps
+        total_ms = max_over_ranks(pg, avg_kernel_ms, dev) * args.steps
     ms_per_step = total_ms / args.steps
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, args.steps, total_ms)
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
 
     # end to end through the public API: pinned host inputs -> device, forward,
@@ -336,12 +357,15 @@ def main():
     o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     qd, kd, vd = (torch.empty_like(q) for _ in range(3))
+    sd = [torch.empty_like(t) for t in scales]
 
     def e2e_step():
         qd.copy_(q_h, non_blocking=True)
         kd.copy_(k_h, non_blocking=True)
         vd.copy_(v_h, non_blocking=True)
-        pkg.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        for dst, src in zip(sd, sc_h):
+            dst.copy_(src, non_blocking=True)
+        forward(qd, kd, vd, sd)
         o_h.copy_(o, non_blocking=True)
         l_h.copy_(lse, non_blocking=True)
 
@@ -357,32 +381,37 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = flops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    e2e_value = job_throughput(flops, world, e2e_steps, e2e_ms)
 
     peaks, peak_src = measured_peaks()
-    peak = float(peaks["bf16_tflops"])
+    # FP8 peak = measured bf16 x 2 (the nominal dense fp8/bf16 ratio, 4.5 / 2.25 PFLOP/s)
+    ratio = 2.0 if fp8 else 1.0
+    peak = float(peaks["bf16_tflops"]) * ratio
+    src = (f"{peak_src} bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json)" if peak_src == "measured"
+           else "fallback 1.9 PFLOP/s bf16") + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else "")
+    kname = {("bf16", 64): "attn_fwd_kernel<64,4,4,false>", ("bf16", 128): "attn_fwd_kernel<128,2,2,false>",
+             ("e4m3", 128): "attn_fwd_kernel<128,3,3,true>"}.get((w.dtype, w.d), "attn_fwd_kernel")
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": traffic_for(w.name),
-            "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3) from MEASURED_PEAKS.json"
-            if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16",
-            "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-            "kernel": "attn_fwd_bf16_kernel", "avg_launch_ms": avg_kernel_ms,
-            "flops_per_launch": flops}
+            "traffic": traffic_for(w.name), "peak_source": src,
+            "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * ratio),
+            "kernel": kname, "avg_launch_ms": avg_kernel_ms, "flops_per_launch": flops}
+    if fp8:
+        # Q K^T runs on the fp8 tensor path and P V on the 16-bit one: the roof of
+        # that mix is flops / (flops/2 / fp8_peak + flops/2 / bf16_peak).
+        mixed = 1.0 / (0.5 / peak + 0.5 / float(peaks["bf16_tflops"]))
+        roof["peak_mixed_fp8_qk_f16_pv"] = mixed
+        roof["frac_of_mixed"] = achieved / mixed
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs)",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) inputs)",
         "config": config_block(args, w),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
-                "h2d_bytes_per_step": int(q_h.nbytes + k_h.nbytes + v_h.nbytes),
+                "h2d_bytes_per_step": int(q_h.nbytes + k_h.nbytes + v_h.nbytes + sum(t.nbytes for t in sc_h)),
                 "d2h_bytes_per_step": int(o_h.nbytes + l_h.nbytes)},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
