@@ -51,7 +51,9 @@ WORKLOAD_TEXT = {
     "cfg3": "bf16 B1 H32 N16384 d128 causal (long sequence, small batch)",
     "cfg4": "bf16 B16 H16 N4096 d64 non-causal, 2 shared Q/K outlier channels x20",
     "cfg5": "e4m3 block-scaled B2 H16 N8192 d128 non-causal, rotated Q/K",
+    "decode": "bf16 B2 H16 Nq512 Nk65536 d128 non-causal, split-K/V forward + merge",
 }
+DECODE = dict(B=2, H=16, Nq=512, Nk=65536, d=128, seed=6)
 
 
 def kernel_hash() -> str:
@@ -156,6 +158,16 @@ def job_throughput(flops_per_step: float, world: int, steps: int, slowest_ms: fl
     return flops_per_step * world * steps / (slowest_ms * 1e-3) / 1e12
 
 
+def make_decode_workload():
+    """Few queries against a long K/V: the K/V rows of a seeded draw and, as
+    queries, its last Nq rows (non-causal)."""
+    c = DECODE
+    w = synth.make_bf16(c["B"], c["H"], c["Nk"], c["d"], False, seed=c["seed"], name="decode")
+    w.q = np.ascontiguousarray(w.q[:, :, c["Nk"] - c["Nq"]:])
+    w.meta["Nq"] = c["Nq"]
+    return w
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -175,7 +187,7 @@ def cpu_oracle_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 256
     for b in range(w.B):
         for h in range(w.H):
             q, k, v = w.head_f64(b, h)
-            rows = synth.sample_rows(w.N, rows_per_head, w.seed, b, h)
+            rows = synth.sample_rows(q.shape[0], rows_per_head, w.seed, b, h)
             t0 = time.perf_counter()
             attention_head(q, k, v, w.causal, w.scale, rows=rows)
             elapsed += time.perf_counter() - t0
@@ -196,7 +208,12 @@ def run_reference(args, world, rank):
     """The oracle timed per step on a bounded sample (rank 0 only)."""
     if rank != 0:
         return
-    w = synth.make_config(args.workload) if not args.small else synth.make_bf16(1, 2, 1024, 128, True, 3)
+    if args.small:
+        w = synth.make_bf16(1, 2, 1024, 128, True, 3)
+    elif args.workload == "decode":
+        w = make_decode_workload()
+    else:
+        w = synth.make_config(args.workload)
     from oracle.attention import attention_head
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     rows_per_step = 32
@@ -204,7 +221,7 @@ def run_reference(args, world, rank):
     def step(i):
         b, h = heads[i % len(heads)]
         q, k, v = w.head_f64(b, h)
-        rows = synth.sample_rows(w.N, rows_per_step, w.seed + i, b, h)
+        rows = synth.sample_rows(q.shape[0], rows_per_step, w.seed + i, b, h)
         t0 = time.perf_counter()
         attention_head(q, k, v, w.causal, w.scale, rows=rows)
         dt = time.perf_counter() - t0
@@ -235,7 +252,9 @@ def run_reference(args, world, rank):
 
 def config_block(args, w):
     in_bytes = w.q.nbytes + w.k.nbytes + w.v.nbytes
+    extra = {"Nq": int(w.q.shape[2]), "splits": args.splits} if w.name == "decode" else {}
     return {"workload": f"{w.name}: {WORKLOAD_TEXT.get(w.name, '')}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            **extra,
             "causal": w.causal, "scale": w.scale, "seed": w.seed,
             "l2": (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB); no flush"
                    if in_bytes > L2_BYTES else
@@ -248,7 +267,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="cfg3", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default="cfg3", choices=sorted(synth.CONFIGS) + ["decode"])
+    ap.add_argument("--splits", type=int, default=16, help="key-range splits of the decode workload")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
@@ -277,9 +297,12 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
+    decode = args.workload == "decode" and not args.custom
     if args.custom:
         B, H, N, d, c = (int(x) for x in args.custom.split(","))
         w = synth.make_bf16(B, H, N, d, bool(c), seed=3, name=f"custom_B{B}H{H}N{N}d{d}{'c' if c else 'n'}")
+    elif decode:
+        w = make_decode_workload()
     else:
         w = synth.make_config(args.workload)
     fp8 = w.dtype == "e4m3"
@@ -292,13 +315,20 @@ def main():
                          for x in (w.q, w.k, w.v))
         sc_h, scales = [], []
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    Nq = q.shape[2]
+    o = torch.empty((w.B, w.H, Nq, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, Nq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     flops = w.flops()
+    if decode:
+        ws = torch.empty(pkg.splitkv_workspace_bytes(w.B, w.H, Nq, w.d, args.splits), dtype=torch.uint8,
+                         device=dev)
 
     def forward(qq, kk, vv, ss):
-        if fp8:
+        if decode:
+            pkg.attn_fwd_splitkv(qq, kk, vv, args.splits, causal=w.causal, scale=w.scale, o=o, lse=lse,
+                                 workspace=ws)
+        elif fp8:
             pkg.attn_fwd_fp8(qq, kk, vv, *ss, causal=w.causal, scale=w.scale, o=o, lse=lse)
         else:
             pkg.attn_fwd(qq, kk, vv, causal=w.causal, scale=w.scale, o=o, lse=lse)
@@ -356,7 +386,7 @@ def main():
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
     o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    qd, kd, vd = (torch.empty_like(q) for _ in range(3))
+    qd, kd, vd = (torch.empty_like(t) for t in (q, k, v))
     sd = [torch.empty_like(t) for t in scales]
 
     def e2e_step():

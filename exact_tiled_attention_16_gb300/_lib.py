@@ -40,6 +40,14 @@ def load_library():
     lib.attn_fwd.restype = ci
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
     lib.attn_fwd_fp8.restype = ci
+    lib.attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, vp]
+    lib.attn_fwd_partial.restype = ci
+    lib.attn_merge.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci, vp, vp, ci, ci, ci, ci, ci, vp]
+    lib.attn_merge.restype = ci
+    lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, ctypes.c_size_t, vp]
+    lib.attn_fwd_splitkv.restype = ci
+    lib.attn_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+    lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_status_string.argtypes = [ci]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_check_device_errors.argtypes = [vp, ctypes.POINTER(ci)]
@@ -135,6 +143,119 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sc
                           B, H, N, d, causal, scale, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8")
+    return o, lse
+
+
+def _check_bf16(*named):
+    import torch
+    for name, t in named:
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [B,H,N,d]")
+
+
+def attn_fwd_partial_raw(q: int, k: int, v: int, o_part: int, lse_part: int, B: int, H: int, Nq: int, Nk: int,
+                         d: int, causal: bool, q_offset: int, k_offset: int, scale: float, stream: int) -> int:
+    return load_library().attn_fwd_partial(q or None, k or None, v or None, o_part or None, lse_part or None,
+                                           B, H, Nq, Nk, d, 1 if causal else 0, q_offset, k_offset,
+                                           float(scale), stream or None)
+
+
+def attn_fwd_partial(q, k, v, causal: bool = False, q_offset: int = 0, k_offset: int = 0,
+                     scale: float | None = None, o_part=None, lse_part=None, stream=None):
+    """Attention of q [B,H,Nq,d] against one K/V shard [B,H,Nk,d] (bf16, CUDA).
+
+    Returns (o_part float32 [B,H,Nq,d], lse_part float32 [B,H,Nq]): the shard's
+    partial result, O normalised by the shard's own sum; rows without a visible
+    key get O = 0 and lse = -inf."""
+    import torch
+    _check_bf16(("q", q), ("k", k), ("v", v))
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != d:
+        raise ValueError("k and v must be [B,H,Nk,d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o_part is None:
+        o_part = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    rc = attn_fwd_partial_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(),
+                              B, H, Nq, Nk, d, causal, q_offset, k_offset, scale, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_partial")
+    return o_part, lse_part
+
+
+def attn_merge_raw(o_parts, lse_parts, o: int, lse: int, out_fp32: bool, B: int, H: int, N: int, d: int,
+                   stream: int) -> int:
+    n = len(o_parts)
+    arr_o = (ctypes.c_void_p * max(1, n))(*[x or None for x in o_parts])
+    arr_l = (ctypes.c_void_p * max(1, n))(*[x or None for x in lse_parts])
+    return load_library().attn_merge(arr_o, arr_l, n, o or None, lse or None, 1 if out_fp32 else 0,
+                                     B, H, N, d, stream or None)
+
+
+def attn_merge(parts, out=None, lse=None, out_fp32: bool = False, stream=None):
+    """Exact merge of partial results [(o_s float32 [B,H,N,d], lse_s float32 [B,H,N]), ...].
+
+    Returns (o, lse); o is bf16 unless out_fp32.  `out`/`lse` may be the first
+    partial's tensors (in-place running merge, out_fp32=True)."""
+    import torch
+    o0, l0 = parts[0]
+    B, H, N, d = o0.shape
+    for o_s, l_s in parts:
+        if o_s.dtype != torch.float32 or l_s.dtype != torch.float32 or o_s.shape != o0.shape \
+                or l_s.shape != l0.shape or not o_s.is_contiguous() or not l_s.is_contiguous():
+            raise ValueError("partials must be contiguous float32 [B,H,N,d] and [B,H,N]")
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=o0.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o0.device)
+    rc = attn_merge_raw([o.data_ptr() for o, _ in parts], [l.data_ptr() for _, l in parts], out.data_ptr(),
+                        lse.data_ptr(), out_fp32, B, H, N, d, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_merge")
+    return out, lse
+
+
+def splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    return int(load_library().attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
+
+
+def attn_fwd_splitkv_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Nq: int, Nk: int, d: int,
+                         causal: bool, scale: float, num_splits: int, workspace: int, workspace_bytes: int,
+                         stream: int) -> int:
+    return load_library().attn_fwd_splitkv(q or None, k or None, v or None, o or None, lse or None, B, H, Nq, Nk,
+                                           d, 1 if causal else 0, float(scale), num_splits, workspace or None,
+                                           int(workspace_bytes), stream or None)
+
+
+def attn_fwd_splitkv(q, k, v, num_splits: int, causal: bool = False, scale: float | None = None, o=None,
+                     lse=None, want_lse: bool = True, workspace=None, stream=None):
+    """Split-K/V attention: q [B,H,Nq,d], k/v [B,H,Nk,d] bf16 CUDA tensors.
+
+    Under the causal mask the queries are the last Nq of the Nk positions.  The
+    scratch workspace (a CUDA tensor of at least splitkv_workspace_bytes bytes)
+    is allocated with torch when not given."""
+    import torch
+    _check_bf16(("q", q), ("k", k), ("v", v))
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    need = splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = attn_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr() if lse is not None else 0, B, H, Nq, Nk, d, causal, scale,
+                              num_splits, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_splitkv")
     return o, lse
 
 

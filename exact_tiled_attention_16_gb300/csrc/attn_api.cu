@@ -11,6 +11,7 @@
 
 #include "../../include/attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_merge.cuh"
 
 namespace {
 
@@ -51,9 +52,10 @@ EncodeTiledFn get_encode() {
   return g_encode;
 }
 
-template <int D, int NK, int NV, bool kFp8>
+template <int D, int NK, int NV, bool kFp8, bool kPartial>
 cudaError_t configure_kernel() {
-  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8, kPartial>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(SmemPlan<D, NK, NV, kFp8>::kBytes));
 }
 
@@ -82,8 +84,11 @@ int device_setup(int* dev_out) {
       st.status = ATTN_ERR_ARCH;
       return;
     }
-    if (configure_kernel<ATTN_BF16_D64>() != cudaSuccess || configure_kernel<ATTN_BF16_D128>() != cudaSuccess ||
-        configure_kernel<ATTN_FP8_D128>() != cudaSuccess ||
+    if (configure_kernel<ATTN_BF16_D64, false>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D128, false>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D64, true>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D128, true>() != cudaSuccess ||
+        configure_kernel<ATTN_FP8_D128, false>() != cudaSuccess ||
         cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_ptr), g_attn_err) != cudaSuccess) {
       st.status = ATTN_ERR_CUDA;
       return;
@@ -111,10 +116,14 @@ int make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, uint32_t
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_OVERFLOW;
 }
 
-int validate_common(const void* q, const void* k, const void* v, const void* o, const void* lse, int B, int H,
-                    int N, int d, float scale) {
+// Largest sequence length accepted: keeps every position and mask limit of the
+// kernels inside 32-bit integers.
+constexpr long long kMaxSeq = 1ll << 30;
+
+int validate_tensors(const void* q, const void* k, const void* v, const void* o, const void* lse, int B, int H,
+                     int Nq, int Nk, int d, float scale) {
   if (!q || !k || !v || !o) return ATTN_ERR_NULL;
-  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_DIMS;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return ATTN_ERR_DIMS;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
   const uintptr_t a = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
@@ -122,35 +131,87 @@ int validate_common(const void* q, const void* k, const void* v, const void* o, 
   if (a & 15u) return ATTN_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_ALIGN;
   const long long BH = static_cast<long long>(B) * H;
-  const long long qblocks = (static_cast<long long>(N) + kBlockM - 1) / kBlockM;
+  const long long qblocks = (static_cast<long long>(Nq) + kBlockM - 1) / kBlockM;
+  if (Nq >= kMaxSeq || Nk >= kMaxSeq) return ATTN_ERR_OVERFLOW;
   if (BH > INT_MAX || BH * qblocks > INT_MAX) return ATTN_ERR_OVERFLOW;
-  // TMA global strides must stay below 2^40 bytes.
-  if (static_cast<long long>(N) * d * 2 >= (1ll << 40)) return ATTN_ERR_OVERFLOW;
   return ATTN_OK;
 }
 
-void fill_params(FwdParams& p, void* o, float* lse, int BH, int N, int causal, float scale, int dev) {
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
+void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset, int k_offset, int num_splits,
+                 float scale, int dev) {
+  std::memset(&p, 0, sizeof(p));
   p.BH = BH;
-  p.N = N;
-  p.num_kblocks = (N + kBlockN - 1) / kBlockN;
-  p.num_pairs = (N + kTilesPerUnit * kBlockM - 1) / (kTilesPerUnit * kBlockM);
-  p.num_units = BH * p.num_pairs;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.q_offset = q_offset;
+  p.k_offset = k_offset;
+  p.num_kblocks = (Nk + kBlockN - 1) / kBlockN;
+  p.num_pairs = (Nq + kTilesPerUnit * kBlockM - 1) / (kTilesPerUnit * kBlockM);
+  if (num_splits > p.num_kblocks) num_splits = p.num_kblocks;
+  if (num_splits < 1) num_splits = 1;
+  p.blocks_per_split = (p.num_kblocks + num_splits - 1) / num_splits;
+  p.num_splits = (p.num_kblocks + p.blocks_per_split - 1) / p.blocks_per_split;
+  p.num_units = BH * p.num_pairs * p.num_splits;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.q_scale = p.k_scale = p.v_scale = nullptr;
   p.timeout_ns = g_timeout_ns;
   p.err = g_dev[dev].err_ptr;
 }
 
-template <int D, int NK, int NV, bool kFp8>
+template <int D, int NK, int NV, bool kFp8, bool kPartial>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p, int dev,
            void* stream) {
   const int grid = p.num_units < g_dev[dev].num_sms ? p.num_units : g_dev[dev].num_sms;
-  attn_fwd_kernel<D, NK, NV, kFp8><<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8>::kBytes,
-                                     static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, p);
+  attn_fwd_kernel<D, NK, NV, kFp8, kPartial><<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8>::kBytes,
+                                               static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// BF16 launch over q [BH, Nq, d], k/v [BH, Nk, d] with the parameters in p;
+// `partial` selects the per-split fp32 output.
+int launch_bf16(const void* q, const void* k, const void* v, int d, bool partial, FwdParams& p, int dev,
+                void* stream) {
+  int rc;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, p.Nq, p.BH, 64)) != ATTN_OK) return rc;
+  if ((rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, p.Nk, p.BH, 64)) != ATTN_OK) return rc;
+  if ((rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, p.Nk, p.BH, 64)) != ATTN_OK) return rc;
+  if (partial) {
+    if (d == 64) return launch<ATTN_BF16_D64, true>(mq, mk, mv, p, dev, stream);
+    return launch<ATTN_BF16_D128, true>(mq, mk, mv, p, dev, stream);
+  }
+  if (d == 64) return launch<ATTN_BF16_D64, false>(mq, mk, mv, p, dev, stream);
+  return launch<ATTN_BF16_D128, false>(mq, mk, mv, p, dev, stream);
+}
+
+int launch_merge(const float* const* o_parts, const float* const* lse_parts, int S, void* out, float* lse_out,
+                 int out_fp32, long long rows, int d, int dev, void* stream) {
+  MergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  for (int s = 0; s < S; ++s) {
+    mp.o[s] = o_parts[s];
+    mp.lse[s] = lse_parts[s];
+  }
+  mp.S = S;
+  mp.out = out;
+  mp.lse_out = lse_out;
+  mp.out_fp32 = out_fp32;
+  mp.rows = rows;
+  const long long warps_needed = rows;
+  long long blocks = (warps_needed + 7) / 8;  // 8 warps per 256-thread block
+  const long long cap = static_cast<long long>(g_dev[dev].num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d == 64) attn_merge_kernel<64><<<static_cast<int>(blocks), 256, 0, st>>>(mp);
+  else attn_merge_kernel<128><<<static_cast<int>(blocks), 256, 0, st>>>(mp);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+size_t splitkv_workspace_bytes(long long BH, long long Nq, long long d, long long S) {
+  const long long rows = BH * Nq;
+  // O partials, then lse partials (each partial's O block stays 16-byte aligned)
+  return static_cast<size_t>(S * rows * d * 4 + S * rows * 4);
 }
 
 }  // namespace
@@ -159,27 +220,22 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              int causal, float scale, int dtype, void* stream) {
-  int rc = validate_common(q, k, v, o, lse, B, H, N, d, scale);
+  int rc = validate_tensors(q, k, v, o, lse, B, H, N, N, d, scale);
   if (rc != ATTN_OK) return rc;
   if (dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
-
-  const int BH = B * H;
-  CUtensorMap mq, mk, mv;
-  if ((rc = make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
-  if ((rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
-  if ((rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, o, lse, BH, N, causal, scale, dev);
-  if (d == 64) return launch<ATTN_BF16_D64>(mq, mk, mv, p, dev, stream);
-  return launch<ATTN_BF16_D128>(mq, mk, mv, p, dev, stream);
+  fill_params(p, B * H, N, N, causal, 0, 0, 1, scale, dev);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  return launch_bf16(q, k, v, d, false, p, dev, stream);
 }
 
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
                  const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
                  void* stream) {
-  int rc = validate_common(q8, k8, v8, o, lse, B, H, N, d, scale);
+  int rc = validate_tensors(q8, k8, v8, o, lse, B, H, N, N, d, scale);
   if (rc != ATTN_OK) return rc;
   if (d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   if (!q_scale || !k_scale || !v_scale) return ATTN_ERR_NULL;
@@ -194,11 +250,85 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map(&mv, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, o, lse, BH, N, causal, scale, dev);
+  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  return launch<ATTN_FP8_D128>(mq, mk, mv, p, dev, stream);
+  return launch<ATTN_FP8_D128, false>(mq, mk, mv, p, dev, stream);
+}
+
+int attn_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,
+                     int Nq, int Nk, int d, int causal, int q_offset, int k_offset, float scale, void* stream) {
+  int rc = validate_tensors(q, k, v, o_part, lse_part, B, H, Nq, Nk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (!lse_part) return ATTN_ERR_NULL;
+  if (q_offset < 0 || k_offset < 0 || q_offset >= kMaxSeq || k_offset >= kMaxSeq) return ATTN_ERR_DIMS;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  FwdParams p;
+  fill_params(p, B * H, Nq, Nk, causal, q_offset, k_offset, 1, scale, dev);
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  return launch_bf16(q, k, v, d, true, p, dev, stream);
+}
+
+int attn_merge(const float* const* o_parts, const float* const* lse_parts, int num_parts, void* o, float* lse,
+               int out_fp32, int B, int H, int N, int d, void* stream) {
+  if (!o_parts || !lse_parts || !o) return ATTN_ERR_NULL;
+  if (num_parts < 1 || num_parts > kMaxMergeParts || B < 1 || H < 1 || N < 1) return ATTN_ERR_DIMS;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  uintptr_t a = reinterpret_cast<uintptr_t>(o);
+  for (int s = 0; s < num_parts; ++s) {
+    if (!o_parts[s] || !lse_parts[s]) return ATTN_ERR_NULL;
+    a |= reinterpret_cast<uintptr_t>(o_parts[s]);
+    if (reinterpret_cast<uintptr_t>(lse_parts[s]) & 3u) return ATTN_ERR_ALIGN;
+  }
+  if ((a & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ALIGN;
+  if (static_cast<long long>(B) * H * N > (1ll << 40)) return ATTN_ERR_OVERFLOW;
+  int dev = 0;
+  int rc = device_setup(&dev);
+  if (rc != ATTN_OK) return rc;
+  return launch_merge(o_parts, lse_parts, num_parts, o, lse, out_fp32 ? 1 : 0,
+                      static_cast<long long>(B) * H * N, d, dev, stream);
+}
+
+size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > kMaxMergeParts) return 0;
+  return splitkv_workspace_bytes(static_cast<long long>(B) * H, Nq, d, num_splits);
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                     int Nk, int d, int causal, float scale, int num_splits, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  int rc = validate_tensors(q, k, v, o, lse, B, H, Nq, Nk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (num_splits < 1 || num_splits > kMaxMergeParts) return ATTN_ERR_DIMS;
+  if (causal && Nq > Nk) return ATTN_ERR_DIMS;
+  if (!workspace) return ATTN_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_ALIGN;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  const int BH = B * H;
+  FwdParams p;
+  // causal: the queries are the last Nq positions of the Nk keys
+  fill_params(p, BH, Nq, Nk, causal, Nk - Nq, 0, num_splits, scale, dev);
+  const long long S = p.num_splits;
+  if (workspace_bytes < splitkv_workspace_bytes(BH, Nq, d, S)) return ATTN_ERR_DIMS;
+  const long long rows = static_cast<long long>(BH) * Nq;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = o_part + S * rows * d;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  if ((rc = launch_bf16(q, k, v, d, true, p, dev, stream)) != ATTN_OK) return rc;
+  const float* op[kMaxMergeParts];
+  const float* lp[kMaxMergeParts];
+  for (int s = 0; s < S; ++s) {
+    op[s] = o_part + s * rows * d;
+    lp[s] = lse_part + s * rows;
+  }
+  return launch_merge(op, lp, static_cast<int>(S), o, lse, 0, rows, d, dev, stream);
 }
 
 const char* attn_status_string(int status) {

@@ -83,13 +83,19 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr float kFp8PScaleLog2 = 6.0f;
 
 struct FwdParams {
-  __nv_bfloat16* o;   // [B*H, N, D]
-  float* lse;         // [B*H, N] or nullptr
+  __nv_bfloat16* o;   // final output: [B*H, Nq, D] bf16
+  float* lse;         // final output: [B*H, Nq] or nullptr
+  float* o_part;      // partial output: [num_splits, B*H, Nq, D] fp32
+  float* lse_part;    // partial output: [num_splits, B*H, Nq] fp32
   int BH;             // B*H
-  int N;
-  int num_kblocks;    // ceil(N / 128)
-  int num_pairs;      // ceil(N / 256): units per (b, h)
-  int num_units;      // BH * num_pairs
+  int Nq, Nk;         // query rows and key rows per head
+  int q_offset;       // causal positions: query i sits at q_offset + i,
+  int k_offset;       //   key j at k_offset + j; j visible to i iff k_pos <= q_pos
+  int num_kblocks;    // ceil(Nk / 128)
+  int num_pairs;      // ceil(Nq / 256)
+  int num_splits;     // key-block ranges per (bh, pair)
+  int blocks_per_split;
+  int num_units;      // BH * num_pairs * num_splits
   int causal;
   float scale_log2;   // scale * log2(e)
   const float* q_scale;  // FP8 only: [B*H, num_kblocks] block scales
@@ -130,11 +136,39 @@ struct SmemPlan {
 
 // Run order: head-major (units of one head are adjacent, so concurrently running
 // units share K/V in L2); under the causal mask each head's pairs run from the
-// heaviest (last rows) to the lightest.
-__device__ __forceinline__ void unit_coords(int u, int num_pairs, int causal, int& bh, int& pair) {
-  bh = u / num_pairs;
-  const int r = u - bh * num_pairs;
-  pair = causal ? (num_pairs - 1 - r) : r;
+// heaviest (last rows) to the lightest; the key-range splits of a pair are
+// adjacent.
+struct UnitInfo {
+  int bh, pair, split;
+  int kb0;   // first K/V block of the unit's key range
+  int n[2];  // K/V blocks tile 0 / tile 1 visit (n[1] >= n[0])
+};
+
+__device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p) {
+  UnitInfo ui;
+  const int per_head = p.num_pairs * p.num_splits;
+  ui.bh = u / per_head;
+  const int r = u - ui.bh * per_head;
+  const int pr = r / p.num_splits;
+  ui.split = r - pr * p.num_splits;
+  ui.pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
+  ui.kb0 = ui.split * p.blocks_per_split;
+  int kb_end = ui.kb0 + p.blocks_per_split;
+  if (kb_end > p.num_kblocks) kb_end = p.num_kblocks;
+#pragma unroll
+  for (int t = 0; t < kTilesPerUnit; ++t) {
+    int hi = kb_end;
+    if (p.causal) {
+      // the last key visible to the tile's last existing row
+      int last_row = (2 * ui.pair + t) * kBlockM + kBlockM - 1;
+      if (last_row > p.Nq - 1) last_row = p.Nq - 1;
+      const int kmax = p.q_offset + last_row - p.k_offset;
+      const int lim = kmax < 0 ? 0 : kmax / kBlockN + 1;
+      if (hi > lim) hi = lim;
+    }
+    ui.n[t] = hi > ui.kb0 ? hi - ui.kb0 : 0;
+  }
+  return ui;
 }
 
 // The unit processed by this CTA in its `round`-th iteration (or -1): position
@@ -145,13 +179,6 @@ __device__ __forceinline__ int unit_for_round(int round, int num_units) {
   const int c = blockIdx.x;
   const int pos = round * G + ((round & 1) ? (G - 1 - c) : c);
   return pos < num_units ? pos : -1;
-}
-
-// K/V blocks that query tile `qt` (128-row block index) needs.
-__device__ __forceinline__ int num_kv_blocks(int qt, const FwdParams& p) {
-  if (!p.causal) return p.num_kblocks;
-  const int lim = qt + 1;  // kBlockM == kBlockN: keys up to the tile's last row
-  return lim < p.num_kblocks ? lim : p.num_kblocks;
 }
 
 // A wait taken by all 32 lanes of a warp that returns the same answer on every
@@ -171,7 +198,10 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D, int NK, int NV, bool kFp8>
+// kPartial selects the output: false = normalised bf16 O and lse (every query
+// row sees key 0: no position offsets, no splits); true = per-split fp32 O and
+// lse, where a tile or row may see no key at all.
+template <int D, int NK, int NV, bool kFp8, bool kPartial>
 __global__ void __launch_bounds__(kNumThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
@@ -258,35 +288,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       uint32_t gk = 0, gv = 0;  // K and V blocks issued so far
-      int units = 0, q_issued = 0;
+      int units = 0, q_issued = 0;  // units with work, Q loads issued
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int u = unit_for_round(round, p.num_units);
         if (u < 0) break;
-        int bh, pair;
-        unit_coords(u, p.num_pairs, p.causal, bh, pair);
-        const int nkv = num_kv_blocks(2 * pair + 1, p);
+        const UnitInfo ui = unit_info(u, p);
+        const int nkv = ui.n[1];
+        if (nkv == 0) continue;  // no visible keys: the softmax warps write the empty result
         if (units > 0 && !(ok = mbar_wait(b_q_empty, (units - 1) & 1, abort_flag, tmo, p.err, 1))) break;
         mbar_arrive_expect_tx(b_q_full, kTilesPerUnit * L::kTileBytes);
         for (int t = 0; t < kTilesPerUnit; ++t)
           for (int c = 0; c < (int)L::kChunks; ++c)
             tma_load_3d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tmap_q, b_q_full, c * L::kChunkElems,
-                        (2 * pair + t) * kBlockM, bh, pol_q);
+                        (2 * ui.pair + t) * kBlockM, ui.bh, pol_q);
         ++q_issued;
         for (int j = 0; j < nkv; ++j) {
+          const int key0 = (ui.kb0 + j) * kBlockN;
           const uint32_t sk = gk % NK, uk = gk / NK;
           if (uk > 0 && !(ok = mbar_wait(b_k_empty + 8 * sk, (uk - 1) & 1, abort_flag, tmo, p.err, 2))) break;
           mbar_arrive_expect_tx(b_k_full + 8 * sk, L::kTileBytes);
           for (int c = 0; c < (int)L::kChunks; ++c)
             tma_load_3d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tmap_k, b_k_full + 8 * sk,
-                        c * L::kChunkElems, j * kBlockN, bh, pol_kv);
+                        c * L::kChunkElems, key0, ui.bh, pol_kv);
           ++gk;
           const uint32_t sv = gv % NV, uv = gv / NV;
           if (uv > 0 && !(ok = mbar_wait(b_v_empty + 8 * sv, (uv - 1) & 1, abort_flag, tmo, p.err, 3))) break;
           mbar_arrive_expect_tx(b_v_full + 8 * sv, L::kTileBytes);
           for (int c = 0; c < (int)L::kChunks; ++c)
             tma_load_3d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tmap_v, b_v_full + 8 * sv,
-                        c * L::kChunkElems, j * kBlockN, bh, pol_kv);
+                        c * L::kChunkElems, key0, ui.bh, pol_kv);
           ++gv;
         }
         ++units;
@@ -344,19 +375,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                      sdesc_sw128(v_base + kk * 16 * 128, LV::kChunkBytes, 1024), idesc_o,
                      (accumulate || kk > 0) ? 1u : 0u);
       };
+      int o_uses[2] = {0, 0};  // units in which tile t has written O_t
       for (int round = 0; ok; ++round) {
         const int u = unit_for_round(round, p.num_units);
         if (u < 0) break;
-        int bh, pair;
-        unit_coords(u, p.num_pairs, p.causal, bh, pair);
-        const int n0 = num_kv_blocks(2 * pair, p);
-        const int n1 = num_kv_blocks(2 * pair + 1, p);
+        const UnitInfo ui = unit_info(u, p);
+        const int n0 = ui.n[0], n1 = ui.n[1];
+        if (n1 == 0) continue;
         if (!(ok = mbar_wait(b_q_full, units & 1, abort_flag, tmo, p.err, 10))) break;
         {
           const uint32_t sk = g % NK;
           if (!(ok = mbar_wait(b_k_full + 8 * sk, (g / NK) & 1, abort_flag, tmo, p.err, 11))) break;
           tc_fence_after();
-          issue_s(0, sk);
+          if (n0 > 0) issue_s(0, sk);
           issue_s(1, sk);
           mma_commit(b_k_empty + 8 * sk);
           if (n1 == 1) mma_commit(b_q_empty);
@@ -377,13 +408,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           }
           for (int t = 0; t < kTilesPerUnit; ++t) {
             const int nt = t == 0 ? n0 : n1;
-            if (j >= nt) continue;
+            if (j >= nt || !ok) continue;
             if (!(ok = mbar_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
             ++p_iter[t];
             if (!(ok = mbar_wait(v_bar, v_par, abort_flag, tmo, p.err, 14))) break;
-            if (j == 0 && units > 0 &&
-                !(ok = mbar_wait(b_o_free + 8 * t, (units - 1) & 1, abort_flag, tmo, p.err, 15 + t)))
-              break;
+            if (j == 0) {
+              // O_t is overwritten: the epilogue of its previous unit must have read it
+              if (o_uses[t] > 0 &&
+                  !(ok = mbar_wait(b_o_free + 8 * t, (o_uses[t] - 1) & 1, abort_flag, tmo, p.err, 15 + t)))
+                break;
+              ++o_uses[t];
+            }
             tc_fence_after();
             issue_pv(t, v_base, j > 0);
             if (j == nt - 1) mma_commit(b_pv_done + 8 * t);
@@ -422,9 +457,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       for (int round = 0; ok; ++round) {
         const int u = unit_for_round(round, p.num_units);
         if (u < 0) break;
-        int bh, pair;
-        unit_coords(u, p.num_pairs, p.causal, bh, pair);
-        const int nkv = num_kv_blocks(2 * pair + 1, p);
+        const int nkv = unit_info(u, p).n[1];
         for (int j = 0; j < nkv && ok; ++j, ++g) {
           const uint32_t sv = g % NV, b = g & 1;
           if (!(ok = mbar_wait(b_v_full + 8 * sv, (g / NV) & 1, abort_flag, tmo, p.err, 30))) break;
@@ -470,11 +503,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     for (int round = 0; ok; ++round) {
       const int u = unit_for_round(round, p.num_units);
       if (u < 0) break;
-      int bh, pair;
-      unit_coords(u, p.num_pairs, p.causal, bh, pair);
-      const int qt = 2 * pair + t;
-      const int nkv = num_kv_blocks(qt, p);
+      const UnitInfo ui = unit_info(u, p);
+      const int bh = ui.bh;
+      const int qt = 2 * ui.pair + t;
+      const int nkv = t == 0 ? ui.n[0] : ui.n[1];
       const int row = qt * kBlockM + row_in_tile;
+      // mask limit of this row relative to a block's first key: key c of block jb is
+      // visible iff c <= row_lim - jb*128 (causal) and jb*128 + c < Nk
+      const int row_lim = p.causal ? (p.q_offset + row - p.k_offset) : 0x3fffffff;
+      const int tile_lim = p.causal ? (p.q_offset + qt * kBlockM - p.k_offset) : 0x3fffffff;  // first row's
       // Exponent multiplier of the raw scores (log2 units); FP8 adds s_q * s_k[j].
       float c_q = p.scale_log2;
       float sv_max = 1.f;
@@ -486,16 +523,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         vs_row = p.v_scale + sb;
         c_q *= __ldg(p.q_scale + sb + (qt < p.num_kblocks ? qt : p.num_kblocks - 1));
         sv_max = 0.f;  // largest V block scale this tile uses (scales are > 0)
-        for (int jj = 0; jj < nkv; ++jj) sv_max = fmaxf(sv_max, __ldg(vs_row + jj));
+        for (int jj = 0; jj < nkv; ++jj) sv_max = fmaxf(sv_max, __ldg(vs_row + ui.kb0 + jj));
       }
       float m_use = -INFINITY;  // running max in log2 units (scale folded in)
       float l = 0.f;            // running normaliser against m_use
       for (int j = 0; j < nkv; ++j) {
+        const int jb = ui.kb0 + j;  // K/V block index
         float cj = c_q;
         float off = 0.f;  // FP8: log2 of the pre-scale and V block-scale ratio
         if constexpr (kFp8) {
-          cj *= __ldg(ks_row + j);
-          off = kFp8PScaleLog2 + lg2_approx(__ldg(vs_row + j) / sv_max);
+          cj *= __ldg(ks_row + jb);
+          off = kFp8PScaleLog2 + lg2_approx(__ldg(vs_row + jb) / sv_max);
         }
         if (!(ok = warp_wait(b_s_full + 8 * t, s_iter & 1, abort_flag, tmo, p.err, 20 + t))) break;
         ++s_iter;
@@ -505,11 +543,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         float s[kBlockN];
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sraw[c]);
-        // mask: causal (key > row) on the diagonal block, keys >= N on the tail block
-        const int key0 = j * kBlockN;
-        if ((p.causal && j == qt) || key0 + kBlockN > p.N) {
-          const int lim_causal = p.causal ? (row - key0) : (kBlockN - 1);
-          const int lim_tail = p.N - 1 - key0;
+        // mask: causal (key position > query position) and keys >= Nk
+        const int key0 = jb * kBlockN;
+        // the block needs a mask iff a key in it lies past the tile's first row or past Nk
+        if (key0 + kBlockN - 1 > tile_lim || key0 + kBlockN > p.Nk) {
+          const int lim_causal = row_lim - key0;
+          const int lim_tail = p.Nk - 1 - key0;
           const int lim = lim_causal < lim_tail ? lim_causal : lim_tail;
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
@@ -570,29 +609,61 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (!(ok = warp_wait(b_pv_done + 8 * t, pv_iter & 1, abort_flag, tmo, p.err, 22 + t))) break;
-      ++pv_iter;
-      tc_fence_after();
-      uint32_t oraw[D];
-      if constexpr (D == 128) tmem_ld128_wait(tO, oraw);
-      else tmem_ld64_wait(tO, oraw);
-      tc_fence_before();
-      mbar_arrive(b_o_free + 8 * t);  // the next unit's first P V may overwrite O_t now
-      const float inv_l = (kFp8 ? sv_max * (1.f / 64.f) : 1.f) / l;
-      if (row < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.N + row) * D);
+      if constexpr (!kPartial) {
+        if (!(ok = warp_wait(b_pv_done + 8 * t, pv_iter & 1, abort_flag, tmo, p.err, 22 + t))) break;
+        ++pv_iter;
+        tc_fence_after();
+        const float inv_l = (kFp8 ? sv_max * (1.f / 64.f) : 1.f) / l;
+        const size_t r = static_cast<size_t>(bh) * p.Nq + row;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + r * D);
+        // O in 64-column halves (fewer live registers); the last load frees O_t
 #pragma unroll
-        for (int v = 0; v < D / 8; ++v) {
-          uint32_t w[4];
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t oraw[64];
+          tmem_ld64_wait(tO + 64 * h, oraw);
+          if (h == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(b_o_free + 8 * t);  // the next unit's first P V may overwrite O_t now
+          }
+          if (row < p.Nq) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * inv_l,
-                               __uint_as_float(oraw[8 * v + 2 * e + 1]) * inv_l);
-          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int v = 0; v < 8; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * inv_l,
+                                   __uint_as_float(oraw[8 * v + 2 * e + 1]) * inv_l);
+              dst[8 * h + v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
         }
-        if (p.lse != nullptr) {
-          // lse = ln(sum_j exp(scale * s_j)) = ln2 * (m_use + log2(l))
-          p.lse[static_cast<size_t>(bh) * p.N + row] = (m_use + lg2_approx(l)) * 0.69314718055994530942f;
+        // lse = ln(sum_j exp(scale * s_j)) = ln2 * (m_use + log2(l))
+        if (row < p.Nq && p.lse != nullptr) p.lse[r] = (m_use + lg2_approx(l)) * 0.69314718055994530942f;
+      } else {
+        uint32_t oraw[D];
+        if (nkv > 0) {
+          if (!(ok = warp_wait(b_pv_done + 8 * t, pv_iter & 1, abort_flag, tmo, p.err, 22 + t))) break;
+          ++pv_iter;
+          tc_fence_after();
+          if constexpr (D == 128) tmem_ld128_wait(tO, oraw);
+          else tmem_ld64_wait(tO, oraw);
+          tc_fence_before();
+          mbar_arrive(b_o_free + 8 * t);
+        } else {
+#pragma unroll
+          for (int c = 0; c < D; ++c) oraw[c] = 0u;
+        }
+        // A row that saw no visible key gets O = 0 and lse = -inf.
+        const bool empty = !(l > 0.f);
+        const float inv_l = empty ? 0.f : 1.f / l;
+        if (row < p.Nq) {
+          const size_t rp = (static_cast<size_t>(ui.split) * p.BH + bh) * p.Nq + row;
+          float4* dst = reinterpret_cast<float4*>(p.o_part + rp * D);
+#pragma unroll
+          for (int v = 0; v < D / 4; ++v)
+            dst[v] = make_float4(__uint_as_float(oraw[4 * v]) * inv_l, __uint_as_float(oraw[4 * v + 1]) * inv_l,
+                                 __uint_as_float(oraw[4 * v + 2]) * inv_l, __uint_as_float(oraw[4 * v + 3]) * inv_l);
+          p.lse_part[rp] = empty ? -INFINITY : (m_use + lg2_approx(l)) * 0.69314718055994530942f;
         }
       }
     }

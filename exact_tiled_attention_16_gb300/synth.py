@@ -199,8 +199,10 @@ class Workload:
     meta: dict = field(default_factory=dict)
 
     def flops(self) -> float:
-        """Counted work: 4*B*H*N^2*d, halved under the causal mask."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        """Counted work: 4*B*H*Nq*N*d (Nq query rows against N keys; Nq = N unless
+        the queries were cut to fewer rows), halved under the square causal mask."""
+        nq = self.q.shape[2]
+        f = 4.0 * self.B * self.H * nq * self.N * self.d
         return f / 2.0 if self.causal else f
 
     def head_f64(self, b: int, h: int):

@@ -34,6 +34,8 @@
 #ifndef ATTN_H_
 #define ATTN_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -88,6 +90,55 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
                  const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
                  void* stream);
+
+/*
+ * attn_fwd_partial -- BF16 attention of queries against ONE key/value shard,
+ * returning the shard's partial result for an exact merge (the blockwise
+ * accumulation of the ring-attention page, "technical insight").
+ *   q          : bf16 [B,H,Nq,d]   (query i sits at position q_offset + i)
+ *   k, v       : bf16 [B,H,Nk,d]   (key j sits at position k_offset + j)
+ *   causal     : nonzero = key j visible to query i iff k_offset + j <= q_offset + i
+ *   o_part     : float32 [B,H,Nq,d] output: O over this shard, normalised by the
+ *                shard's own softmax sum (16-byte aligned)
+ *   lse_part   : float32 [B,H,Nq] output: ln of the shard's sum of exp(scores);
+ *                a row with no visible key gets o_part = 0 and lse_part = -inf
+ *   q_offset, k_offset : >= 0;  d : 64 or 128;  other arguments as attn_fwd.
+ */
+int attn_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,
+                     int Nq, int Nk, int d, int causal, int q_offset, int k_offset, float scale, void* stream);
+
+/*
+ * attn_merge -- exact merge of num_parts partial results over disjoint key sets:
+ *   lse = ln sum_s exp(lse_s),  O = sum_s exp(lse_s - lse) O_s.
+ *   o_parts, lse_parts : HOST arrays of num_parts (1..16) DEVICE pointers to
+ *                        float32 [B,H,N,d] (16-byte aligned) and [B,H,N]
+ *   o        : output [B,H,N,d], bf16 (out_fp32 = 0) or float32 (out_fp32 != 0);
+ *              may be o_parts[0] when out_fp32 (in-place running merge)
+ *   lse      : float32 [B,H,N] output or NULL; may be lse_parts[0]
+ * Rows whose partials are all empty (lse = -inf) get O = 0 and lse = -inf.
+ */
+int attn_merge(const float* const* o_parts, const float* const* lse_parts, int num_parts, void* o, float* lse,
+               int out_fp32, int B, int H, int N, int d, void* stream);
+
+/*
+ * attn_fwd_splitkv -- BF16 attention with the keys split into num_splits
+ * contiguous ranges processed as separate work units (more parallelism when
+ * there are few query tiles), followed by attn_merge.
+ *   q : bf16 [B,H,Nq,d];  k, v : bf16 [B,H,Nk,d];  o : bf16 [B,H,Nq,d];
+ *   lse : float32 [B,H,Nq] or NULL
+ *   causal : the queries are the LAST Nq positions of the Nk keys (query i at
+ *            position Nk - Nq + i; requires Nq <= Nk); Nq = Nk is attn_fwd's mask
+ *   num_splits : 1..16 (reduced if there are fewer 128-key blocks)
+ *   workspace : device scratch of at least attn_splitkv_workspace_bytes(...)
+ *               bytes, 16-byte aligned, owned by the caller; its contents on
+ *               entry do not matter
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                     int Nk, int d, int causal, float scale, int num_splits, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Scratch bytes attn_fwd_splitkv needs (0 for invalid arguments). */
+size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
 
 /* Human-readable name of an attn_status value (static storage). */
 const char* attn_status_string(int status);

@@ -93,6 +93,32 @@ def test_fp8_validation_codes(lib):
     assert _call_fp8(lib, scale=0.0) == -10
 
 
+def test_partial_merge_splitkv_validation(lib):
+    import exact_tiled_attention_16_gb300._lib as L
+    P = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000)
+    # partial: lse_part required, offsets >= 0
+    assert L.attn_fwd_partial_raw(P["q"], P["k"], P["v"], P["o"], 0, 1, 1, 128, 128, 64, 0, 0, 0, 0.1, 0) == -1
+    assert L.attn_fwd_partial_raw(P["q"], P["k"], P["v"], P["o"], P["lse"], 1, 1, 128, 128, 64, 1, -1, 0, 0.1,
+                                  0) == -2
+    assert L.attn_fwd_partial_raw(P["q"], P["k"], P["v"], P["o"], P["lse"], 1, 1, 128, 0, 64, 0, 0, 0, 0.1, 0) == -2
+    # merge: part count, alignment, head dim
+    assert L.attn_merge_raw([], [], P["o"], P["lse"], True, 1, 1, 8, 64, 0) == -2
+    assert L.attn_merge_raw([0x1000] * 17, [0x2000] * 17, P["o"], P["lse"], True, 1, 1, 8, 64, 0) == -2
+    assert L.attn_merge_raw([0x1008], [0x2000], P["o"], P["lse"], True, 1, 1, 8, 64, 0) == -5
+    assert L.attn_merge_raw([0x1000], [0x2000], P["o"], P["lse"], True, 1, 1, 8, 96, 0) == -3
+    assert L.attn_merge_raw([0], [0x2000], P["o"], P["lse"], True, 1, 1, 8, 64, 0) == -1
+    # split-K/V: workspace, split count, causal needs Nq <= Nk
+    assert L.attn_fwd_splitkv_raw(P["q"], P["k"], P["v"], P["o"], P["lse"], 1, 1, 128, 256, 64, 0, 0.1, 2, 0,
+                                  1 << 20, 0) == -1
+    assert L.attn_fwd_splitkv_raw(P["q"], P["k"], P["v"], P["o"], P["lse"], 1, 1, 128, 256, 64, 0, 0.1, 0,
+                                  0x6000, 1 << 20, 0) == -2
+    assert L.attn_fwd_splitkv_raw(P["q"], P["k"], P["v"], P["o"], P["lse"], 1, 1, 300, 256, 64, 1, 0.1, 2,
+                                  0x6000, 1 << 20, 0) == -2
+    # workspace size: S * B*H*Nq * (d + 1) * 4 bytes
+    assert L.splitkv_workspace_bytes(2, 3, 100, 64, 4) == 4 * 6 * 100 * 65 * 4
+    assert L.splitkv_workspace_bytes(1, 1, 1, 96, 1) == 0
+
+
 def test_wait_timeout_setter(lib):
     assert lib.attn_set_wait_timeout_ns(10) == -2
     assert lib.attn_set_wait_timeout_ns(4_000_000_000) == 0
