@@ -345,6 +345,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_ARCH: return "ATTN_ERR_ARCH: the current device is not sm_103";
     case ATTN_ERR_SCALE: return "ATTN_ERR_SCALE: scale must be finite and > 0";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA call failed (no device?)";
+    case ATTN_ERR_SCRATCH: return "ATTN_ERR_SCRATCH: the problem needs more than the library's fixed scratch";
     default: return "unknown attn_status";
   }
 }
@@ -395,3 +396,66 @@ extern "C" int attn_selftest_wait_timeout(void* stream) {
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return attn_check_device_errors(stream, nullptr);
 }
+
+// ---------------------------------------------------------------------------
+// Split-K/V attention for callers that cannot allocate device memory.
+//
+// Some callers may not request device memory at all: a serving loop whose
+// memory is owned by another allocator (a framework's caching allocator or a
+// pool reserved at start-up) and which has no handle on it, or a latency-critical
+// path where a cudaMalloc, which can synchronise the device, is not acceptable.
+// For them this entry point takes its scratch from a fixed array compiled into
+// the library instead of from the caller.
+//
+// The array is a file-scope __device__ variable of kStaticScratchBytes: every GPU
+// that loads the library holds it until the process exits.  Host code cannot use
+// the variable's name as a device address; its address is obtained once per
+// device with cudaGetSymbolAddress (with that device current) the first time the
+// entry point runs there, so the first call on each device should happen before
+// any stream capture.  All calls share the one array and it keeps the contents
+// of the last call: the kernels overwrite every partial result they later read,
+// so nothing has to be cleared, but two calls that overlap on the GPU (e.g. on
+// different streams) race on it and must not be issued.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
+__device__ __align__(256) unsigned char g_splitkv_static_scratch[kStaticScratchBytes];
+
+struct StaticScratch {
+  std::once_flag once;
+  int status = ATTN_ERR_CUDA;
+  void* ptr = nullptr;
+};
+StaticScratch g_static_scratch[kMaxDevices];
+}  // namespace
+
+extern "C" int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                       int H, int Nq, int Nk, int d, int causal, float scale, int num_splits,
+                                       void* stream) {
+  int rc = validate_tensors(q, k, v, o, lse, B, H, Nq, Nk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (num_splits < 1 || num_splits > kMaxMergeParts) return ATTN_ERR_DIMS;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  StaticScratch& sc = g_static_scratch[dev];
+  std::call_once(sc.once, [&sc] {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_splitkv_static_scratch) == cudaSuccess && ptr != nullptr) {
+      sc.ptr = ptr;
+      sc.status = ATTN_OK;
+    }
+  });
+  if (sc.status != ATTN_OK) return sc.status;
+  // the number of splits attn_fwd_splitkv will use (it never uses more than the
+  // key blocks allow), and the scratch those need
+  const int nkb = (Nk + kBlockN - 1) / kBlockN;
+  const int s_req = num_splits < nkb ? num_splits : nkb;
+  const int per = (nkb + s_req - 1) / s_req;
+  const int s_eff = (nkb + per - 1) / per;
+  if (splitkv_workspace_bytes(static_cast<long long>(B) * H, Nq, d, s_eff) > kStaticScratchBytes)
+    return ATTN_ERR_SCRATCH;
+  return attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, num_splits, sc.ptr,
+                          kStaticScratchBytes, stream);
+}
+
+extern "C" size_t attn_splitkv_static_scratch_bytes(void) { return kStaticScratchBytes; }

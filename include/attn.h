@@ -52,7 +52,8 @@ typedef enum {
   ATTN_ERR_TIMEOUT = -8,             /* a bounded in-kernel wait ran out (see attn_check_device_errors) */
   ATTN_ERR_ARCH = -9,                /* the current device is not sm_103 */
   ATTN_ERR_SCALE = -10,              /* scale not finite and > 0 */
-  ATTN_ERR_CUDA = -11                /* a CUDA runtime/driver call failed (e.g. no device) */
+  ATTN_ERR_CUDA = -11,               /* a CUDA runtime/driver call failed (e.g. no device) */
+  ATTN_ERR_SCRATCH = -12             /* attn_fwd_splitkv_static: the problem needs more than its fixed scratch */
 } attn_status;
 
 typedef enum { ATTN_BF16 = 0 } attn_dtype;
@@ -139,6 +140,35 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
 
 /* Scratch bytes attn_fwd_splitkv needs (0 for invalid arguments). */
 size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/*
+ * attn_fwd_splitkv_static -- attn_fwd_splitkv without a workspace argument, for
+ * callers that cannot allocate device memory.  The pages have no counterpart:
+ * this is a convenience of the library, not part of the method.
+ *
+ * Who needs it: code that may not request device memory itself -- for example a
+ * serving loop whose GPU memory belongs to another allocator (a framework's
+ * caching allocator, or a pool reserved at start-up) and which holds no handle
+ * on it, or a latency-critical path where cudaMalloc, which can synchronise the
+ * device, is not allowed.  Such a caller passes only inputs and outputs; the
+ * scratch for the partial results comes from a fixed array compiled into the
+ * library (attn_splitkv_static_scratch_bytes() bytes, 32 MiB), which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Arguments as attn_fwd_splitkv.  Returns ATTN_ERR_SCRATCH, launching nothing,
+ * when num_splits * B*H*Nq * (d + 1) * 4 bytes exceed that size (num_splits as
+ * reduced to the number of 128-key blocks).  Nothing in this function allocates
+ * memory.  The first call on a device looks up the array's device address; make
+ * that first call before any stream capture.  All calls share the array (it keeps
+ * the last call's contents; every value is rewritten before it is read, so nothing
+ * needs clearing): calls whose kernels may overlap on the GPU, such as calls on
+ * two streams without ordering between them, race on it and must be avoided.
+ */
+int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int Nq, int Nk, int d, int causal, float scale, int num_splits, void* stream);
+
+/* Size in bytes of the fixed scratch attn_fwd_splitkv_static uses. */
+size_t attn_splitkv_static_scratch_bytes(void);
 
 /* Human-readable name of an attn_status value (static storage). */
 const char* attn_status_string(int status);
