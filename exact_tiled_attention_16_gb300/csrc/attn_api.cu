@@ -153,6 +153,11 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
   p.num_splits = (p.num_kblocks + p.blocks_per_split - 1) / p.blocks_per_split;
   p.num_units = BH * p.num_pairs * p.num_splits;
   p.causal = causal ? 1 : 0;
+  // zigzag pairing balances causal work but halves the number of items dealt to
+  // CTAs; with fewer than four rounds of them the last, partly empty round costs
+  // more than the balance gains
+  const long long combined = static_cast<long long>(BH) * ((p.num_pairs + 1) / 2);
+  p.zigzag = (causal && p.num_splits == 1 && combined >= 4ll * g_dev[dev].num_sms) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = g_dev[dev].err_ptr;
@@ -161,7 +166,9 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
 template <int D, int NK, int NV, bool kFp8, bool kPartial>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p, int dev,
            void* stream) {
-  const int grid = p.num_units < g_dev[dev].num_sms ? p.num_units : g_dev[dev].num_sms;
+  // work items dealt to CTAs: units, or combined heavy+light pairs under zigzag
+  const int items = p.zigzag ? p.BH * ((p.num_pairs + 1) / 2) : p.num_units;
+  const int grid = items < g_dev[dev].num_sms ? items : g_dev[dev].num_sms;
   attn_fwd_kernel<D, NK, NV, kFp8, kPartial><<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8>::kBytes,
                                                static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;

@@ -97,6 +97,7 @@ struct FwdParams {
   int blocks_per_split;
   int num_units;      // BH * num_pairs * num_splits
   int causal;
+  int zigzag;         // causal, unsplit: balanced heavy+light pairing of units
   float scale_log2;   // scale * log2(e)
   const float* q_scale;  // FP8 only: [B*H, num_kblocks] block scales
   const float* k_scale;
@@ -171,14 +172,36 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p) {
   return ui;
 }
 
-// The unit processed by this CTA in its `round`-th iteration (or -1): position
-// c of each round on even rounds, the mirror position on odd rounds, so that
-// heavy and light causal units interleave across CTAs.
-__device__ __forceinline__ int unit_for_round(int round, int num_units) {
+constexpr int kNoMoreUnits = -1;
+constexpr int kSkipRound = -2;
+
+// The unit this CTA processes in its `round`-th iteration, kNoMoreUnits when it
+// is done, or kSkipRound for an iteration without a unit (every role skips it).
+//
+// Causal, unsplit: "zigzag" pairing.  Pair p of a head costs about 4p+3 K/V
+// blocks, so the heavy pair P-1-c and the light pair c together cost the same
+// for every c.  Combined unit k = (head, c) goes to CTA k mod G; the CTA runs its
+// heavy pair in the even iteration and its light pair in the odd one (an odd
+// pair count leaves the middle pair alone).  Combined units of one head are
+// adjacent, so the CTAs running at a time share a few heads' K/V in L2.
+// Otherwise: position c of each round on even rounds and the mirror position on
+// odd rounds (the units of a head are adjacent).
+__device__ __forceinline__ int unit_for_round(int round, const FwdParams& p) {
   const int G = gridDim.x;
   const int c = blockIdx.x;
+  if (p.zigzag) {
+    const int half = (p.num_pairs + 1) >> 1;
+    const int k = (round >> 1) * G + c;
+    if (k >= p.BH * half) return kNoMoreUnits;
+    const int bh = k / half;
+    const int cc = k - bh * half;
+    const int heavy = p.num_pairs - 1 - cc;
+    if ((round & 1) && heavy == cc) return kSkipRound;
+    const int pair = (round & 1) ? cc : heavy;
+    return bh * p.num_pairs + (p.num_pairs - 1 - pair);  // unit id as unit_info decodes it
+  }
   const int pos = round * G + ((round & 1) ? (G - 1 - c) : c);
-  return pos < num_units ? pos : -1;
+  return pos < p.num_units ? pos : kNoMoreUnits;
 }
 
 // A wait taken by all 32 lanes of a warp that returns the same answer on every
@@ -291,8 +314,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       int units = 0, q_issued = 0;  // units with work, Q loads issued
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round, p.num_units);
-        if (u < 0) break;
+        const int u = unit_for_round(round, p);
+        if (u == kNoMoreUnits) break;
+        if (u == kSkipRound) continue;
         const UnitInfo ui = unit_info(u, p);
         const int nkv = ui.n[1];
         if (nkv == 0) continue;  // no visible keys: the softmax warps write the empty result
@@ -377,8 +401,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       };
       int o_uses[2] = {0, 0};  // units in which tile t has written O_t
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round, p.num_units);
-        if (u < 0) break;
+        const int u = unit_for_round(round, p);
+        if (u == kNoMoreUnits) break;
+        if (u == kSkipRound) continue;
         const UnitInfo ui = unit_info(u, p);
         const int n0 = ui.n[0], n1 = ui.n[1];
         if (n1 == 0) continue;
@@ -455,8 +480,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       uint32_t g = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round, p.num_units);
-        if (u < 0) break;
+        const int u = unit_for_round(round, p);
+        if (u == kNoMoreUnits) break;
+        if (u == kSkipRound) continue;
         const int nkv = unit_info(u, p).n[1];
         for (int j = 0; j < nkv && ok; ++j, ++g) {
           const uint32_t sv = g % NV, b = g & 1;
@@ -501,8 +527,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     uint32_t s_iter = 0, pv_iter = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
-      const int u = unit_for_round(round, p.num_units);
-      if (u < 0) break;
+      const int u = unit_for_round(round, p);
+      if (u == kNoMoreUnits) break;
+      if (u == kSkipRound) continue;
       const UnitInfo ui = unit_info(u, p);
       const int bh = ui.bh;
       const int qt = 2 * ui.pair + t;

@@ -186,3 +186,21 @@ def test_torch_streams():
     s.synchronize()
     assert_bf16_tol(compare_rows(w, o.float().cpu().numpy().astype(np.float64),
                                  lse.cpu().numpy().astype(np.float64)), "side stream")
+
+
+@pytest.mark.parametrize("shape", [(8, 76, 512, 128), (4, 76, 640, 64)], ids=["pairs2", "pairs3_odd"])
+def test_zigzag_schedule_covers_every_unit(shape):
+    """Causal launches with at least four rounds of combined heavy+light pair
+    units take the zigzag schedule; every row must be written and correct (an
+    odd pair count leaves the middle pair of each head on its own)."""
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d = shape
+    w = synth.make_bf16(B, H, N, d, True, seed=77 + N)
+    q, k, v = to_device(w)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    pkg.attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o.float()).any() and not torch.isnan(lse).any()
+    assert_bf16_tol(compare_rows(w, o.float().cpu().numpy().astype(np.float64),
+                                 lse.cpu().numpy().astype(np.float64)), f"zigzag {shape}")
