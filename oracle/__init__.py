@@ -4,3 +4,4 @@ Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
 this package.  The library's compute path never calls it.
 """
 from .attention import attention_head, attention, attention_probs  # noqa: F401
+from .attention_bwd import attention_bwd_head, attention_bwd  # noqa: F401
