@@ -1,4 +1,4 @@
-"""Exact tiled attention forward pass for one GB300 (sm_103a).
+"""Exact tiled attention (forward and backward) for one GB300 (sm_103a).
 
 The compute path is the shared library built from ``csrc/`` (``libattn.so``):
 hand-written tcgen05/TMA kernels behind a C ABI (``include/attn.h``).  This
@@ -12,6 +12,7 @@ from __future__ import annotations
 __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_fp8", "attn_fwd_fp8_raw", "attn_status_string", "load_library", "AttnError",
            "attn_fwd_partial", "attn_fwd_partial_raw", "attn_merge", "attn_merge_raw",
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
+           "attn_bwd", "attn_bwd_raw", "bwd_workspace_bytes",
            "check_device_errors", "set_wait_timeout_ns", "selftest_wait_timeout"]
 
 

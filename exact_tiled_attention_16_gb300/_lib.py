@@ -48,6 +48,10 @@ def load_library():
     lib.attn_fwd_splitkv.restype = ci
     lib.attn_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
     lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, ctypes.c_size_t, vp]
+    lib.attn_bwd.restype = ci
+    lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_status_string.argtypes = [ci]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_check_device_errors.argtypes = [vp, ctypes.POINTER(ci)]
@@ -257,6 +261,48 @@ def attn_fwd_splitkv(q, k, v, num_splits: int, causal: bool = False, scale: floa
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_splitkv")
     return o, lse
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(load_library().attn_bwd_workspace_bytes(B, H, N))
+
+
+def attn_bwd_raw(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int, H: int,
+                 N: int, d: int, causal: bool, scale: float, workspace: int, workspace_bytes: int,
+                 stream: int) -> int:
+    return load_library().attn_bwd(q or None, k or None, v or None, o or None, dout or None, lse or None,
+                                   dq or None, dk or None, dv or None, B, H, N, d, 1 if causal else 0,
+                                   float(scale), workspace or None, int(workspace_bytes), stream or None)
+
+
+def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None,
+             dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for bf16 CUDA tensors [B,H,N,d].
+
+    o and lse are attn_fwd's outputs for the same q, k, v, causal flag and scale;
+    dout is the gradient of o.  The workspace (a CUDA tensor of at least
+    bwd_workspace_bytes bytes) is allocated with torch when not given."""
+    import torch
+    _check_bf16(("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout))
+    if any(t.shape != q.shape for t in (k, v, o, dout)):
+        raise ValueError("q, k, v, o and dout must have the same shape [B,H,N,d]")
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be a contiguous CUDA float32 tensor [B,H,N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = attn_bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, causal, scale,
+                      workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def check_device_errors(stream=None):

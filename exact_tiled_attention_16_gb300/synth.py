@@ -30,6 +30,7 @@ STREAM_Q, STREAM_K, STREAM_V = 0, 1, 2
 STREAM_OUTLIER_QK, STREAM_OUTLIER_V = 3, 4
 STREAM_ROTATION = 5
 STREAM_ROWS = 6
+STREAM_DO = 7
 
 E4M3_MAX = 448.0
 FP8_BLOCK = 128  # tokens per quantisation block
@@ -234,6 +235,12 @@ def make_bf16(B, H, N, d, causal, seed, scale=None, qk_outlier_frac=0.0, qk_outl
         scale = 1.0 / math.sqrt(d)
     return Workload(name, "bf16", B, H, N, d, bool(causal), float(scale), seed,
                     f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v), meta=meta)
+
+
+def make_grad_out(B, H, N, d, seed) -> np.ndarray:
+    """Upstream gradient dO [B,H,N,d] for the backward pass: i.i.d. N(0,1)
+    (float32 draw, bf16 RNE bits), on its own stream of the workload's seed."""
+    return f32_to_bf16_bits(normal_f32((B, H, N, d), seed, STREAM_DO))
 
 
 def make_fp8(B, H, N, d, causal, seed, scale=None, outlier_frac=0.01, outlier_mult=10.0,

@@ -170,6 +170,27 @@ int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o
 /* Size in bytes of the fixed scratch attn_fwd_splitkv_static uses. */
 size_t attn_splitkv_static_scratch_bytes(void);
 
+/*
+ * attn_bwd -- gradients of the BF16 attention forward (the training use the
+ * FlashAttention-2 article reports under "Performance"):
+ *   dV = P^T dO,  dS = P o (dP - D) with dP = dO V^T and D_i = do_i . o_i,
+ *   dQ = scale dS K,  dK = scale dS^T Q,
+ * with P recomputed tile by tile from the forward pass's log-sum-exp.
+ *   q, k, v, o, dout : const bf16 [B,H,N,d] (o and lse from attn_fwd with the
+ *                      same inputs, causal flag and scale), 16-byte aligned
+ *   lse              : const float32 [B,H,N]
+ *   dq, dk, dv       : bf16 [B,H,N,d] outputs, 16-byte aligned
+ *   workspace        : device scratch of at least attn_bwd_workspace_bytes(B,H,N)
+ *                      bytes (4-byte aligned), owned by the caller
+ *   d : 64 or 128; other arguments as attn_fwd.  Deterministic (no atomics).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/* Scratch bytes attn_bwd needs (0 for invalid arguments). */
+size_t attn_bwd_workspace_bytes(int B, int H, int N);
+
 /* Human-readable name of an attn_status value (static storage). */
 const char* attn_status_string(int status);
 

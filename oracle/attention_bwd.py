@@ -50,3 +50,39 @@ def attention_bwd(q, k, v, do, causal, scale):
             dq, dk, dv = attention_bwd_head(q[b, h], k[b, h], v[b, h], do[b, h], causal, scale)
             out[0][b, h], out[1][b, h], out[2][b, h] = dq, dk, dv
     return tuple(out)
+
+
+def _grad_rows(q, k, v, do, causal, scale, rows):
+    """p, dp and ds for the query positions `rows` (every key), per the
+    definitions above; each row depends only on its own scores."""
+    p = attention_probs(q, k, causal, scale, rows)
+    dp = do[rows] @ v.T
+    d_row = (p * dp).sum(axis=1, keepdims=True)
+    return p, p * (dp - d_row)
+
+
+def attention_bwd_query_rows(q, k, v, do, causal, scale, rows):
+    """dq for the query positions `rows` only -> [R, d] float64."""
+    q, k, v, do = (np.asarray(x, np.float64) for x in (q, k, v, do))
+    rows = np.asarray(rows, np.int64)
+    _, ds = _grad_rows(q, k, v, do, causal, scale, rows)
+    return scale * (ds @ k)
+
+
+def attention_bwd_key_rows(q, k, v, do, causal, scale, keys, row_chunk=2048):
+    """(dk, dv) for the key positions `keys` only -> two [K, d] float64 arrays.
+
+    Column j of P needs every query row's normaliser, so every row of P and dS is
+    formed (row_chunk query rows at a time, each row exactly as in
+    attention_bwd_head) and only the requested columns are kept."""
+    q, k, v, do = (np.asarray(x, np.float64) for x in (q, k, v, do))
+    keys = np.asarray(keys, np.int64)
+    n = q.shape[0]
+    p_cols = np.empty((n, keys.size))
+    ds_cols = np.empty((n, keys.size))
+    for r0 in range(0, n, row_chunk):
+        rows = np.arange(r0, min(n, r0 + row_chunk))
+        p, ds = _grad_rows(q, k, v, do, causal, scale, rows)
+        p_cols[rows] = p[:, keys]
+        ds_cols[rows] = ds[:, keys]
+    return scale * (ds_cols.T @ q), p_cols.T @ do

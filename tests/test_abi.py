@@ -119,6 +119,30 @@ def test_partial_merge_splitkv_validation(lib):
     assert L.splitkv_workspace_bytes(1, 1, 1, 96, 1) == 0
 
 
+def test_bwd_validation(lib):
+    import exact_tiled_attention_16_gb300._lib as L
+    a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, dout=0x5000, lse=0x6000, dq=0x7000, dk=0x8000, dv=0x9000,
+             B=1, H=2, N=100, d=64, causal=1, scale=0.125, workspace=0xa000, workspace_bytes=800)
+
+    def call(**kw):
+        x = dict(a)
+        x.update(kw)
+        return L.attn_bwd_raw(x["q"], x["k"], x["v"], x["o"], x["dout"], x["lse"], x["dq"], x["dk"], x["dv"],
+                              x["B"], x["H"], x["N"], x["d"], x["causal"], x["scale"], x["workspace"],
+                              x["workspace_bytes"], 0)
+    for name in ("q", "o", "dout", "lse", "dq", "dk", "dv", "workspace"):
+        assert call(**{name: 0}) == -1, name
+    assert call(N=0) == -2
+    assert call(d=96) == -3
+    assert call(scale=0.0) == -10
+    assert call(dout=0x5008) == -5
+    assert call(dk=0x8002) == -5
+    assert call(lse=0x6002) == -5
+    assert call(workspace_bytes=799) == -2  # D vector: B*H*N floats
+    assert L.bwd_workspace_bytes(1, 2, 100) == 800
+    assert L.bwd_workspace_bytes(0, 2, 100) == 0
+
+
 def test_wait_timeout_setter(lib):
     assert lib.attn_set_wait_timeout_ns(10) == -2
     assert lib.attn_set_wait_timeout_ns(4_000_000_000) == 0

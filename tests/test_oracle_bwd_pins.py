@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from oracle.attention import attention_head
-from oracle.attention_bwd import attention_bwd_head
+from oracle.attention_bwd import attention_bwd_head, attention_bwd_key_rows, attention_bwd_query_rows
 
 
 def _loss(q, k, v, do, causal, scale):
@@ -82,6 +82,25 @@ ALL_CHECKS = [check_finite_differences, check_torch_autograd, check_invariants]
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
 def test_bwd_oracle_pin(check):
     check(attention_bwd_head)
+
+
+def _sampled(q, k, v, do, causal, scale):
+    """The sampled-output oracle asked for every row and key (in an odd order,
+    with a row chunk that splits the rows unevenly) must meet the same pins."""
+    n = np.asarray(q).shape[0]
+    order = np.random.default_rng(3).permutation(n)
+    dq = np.empty((n, np.asarray(q).shape[1]))
+    dq[order] = attention_bwd_query_rows(q, k, v, do, causal, scale, order)
+    dk_s, dv_s = attention_bwd_key_rows(q, k, v, do, causal, scale, order, row_chunk=7)
+    dk = np.empty_like(dq)
+    dv = np.empty((n, np.asarray(v).shape[1]))
+    dk[order], dv[order] = dk_s, dv_s
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
+def test_sampled_bwd_oracle_pin(check):
+    check(_sampled)
 
 
 def _broken(kind):
