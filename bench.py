@@ -5,6 +5,11 @@ One step = one call of the library's attention forward over the whole workload
 P V, epilogue) with inputs resident in HBM.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3] [--impl ours|reference]
+                  [--pass fwd|bwd]
+
+--pass bwd times the backward instead (one step = one attn_bwd call: D prep, dQ
+pass, dK/dV pass) on O and LSE from one untimed forward and a seeded dO; its
+work is counted as 2.5x the forward's (five N x N x d products instead of two).
 
 Multi-GPU: the forward pass of independent problems has no exchange step, so
 N > 1 runs N independent replicas (one per rank, launched by torchrun); value is
@@ -40,8 +45,11 @@ sys.path.insert(0, ROOT)
 from exact_tiled_attention_16_gb300 import synth  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense BF16/FP8 tensor peak"
+METRIC_BWD = "attention bwd TFLOP/s on 1 GB300 (counted as 2.5x forward flops) and % of dense BF16 tensor peak"
+BWD_FLOP_RATIO = 2.5
 L2_BYTES = 126 * 1024 * 1024
 KERNEL_SOURCES = ["exact_tiled_attention_16_gb300/csrc/attn_fwd_kernel.cuh",
+                  "exact_tiled_attention_16_gb300/csrc/attn_bwd_kernel.cuh",
                   "exact_tiled_attention_16_gb300/csrc/ptx.cuh",
                   "exact_tiled_attention_16_gb300/csrc/attn_api.cu"]
 WORKLOAD_TEXT = {
@@ -204,6 +212,37 @@ def cpu_oracle_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 256
     return flops / elapsed / 1e12, desc, elapsed
 
 
+def cpu_oracle_bwd_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 128, max_heads=None):
+    """Times the fp64 gradient oracle's dq on sampled query rows of successive
+    heads until budget_s seconds have passed.  Each row is counted as its share of
+    the backward's work (2.5x its forward flops), so the rate is in the same
+    units as the GPU number."""
+    from oracle.attention_bwd import attention_bwd_query_rows
+    flops = elapsed = 0.0
+    heads = rows_done = 0
+    done = False
+    for b in range(w.B):
+        for h in range(w.H):
+            q, k, v = w.head_f64(b, h)
+            do = synth.bf16_bits_to_f64(synth.make_grad_out(1, 1, w.N, w.d, seed=w.seed + 1000 * b + h)[0, 0])
+            rows = synth.sample_rows(q.shape[0], rows_per_head, w.seed, b, h)
+            t0 = time.perf_counter()
+            attention_bwd_query_rows(q, k, v, do, w.causal, w.scale, rows)
+            elapsed += time.perf_counter() - t0
+            vis = (rows + 1) if w.causal else np.full(len(rows), w.N)
+            flops += BWD_FLOP_RATIO * float(4.0 * w.d * vis.sum())
+            heads += 1
+            rows_done += len(rows)
+            done = elapsed >= budget_s or bool(max_heads and heads >= max_heads)
+            if done:
+                break
+        if done:
+            break
+    desc = (f"dq of {rows_done} query rows ({rows_per_head} seeded rows per head x {heads} heads) of "
+            f"{w.name}, each counted as 2.5x its forward flops; fp64 numpy, {_CORES} BLAS threads")
+    return flops / elapsed / 1e12, desc, elapsed
+
+
 def run_reference(args, world, rank):
     """The oracle timed per step on a bounded sample (rank 0 only)."""
     if rank != 0:
@@ -215,18 +254,25 @@ def run_reference(args, world, rank):
     else:
         w = synth.make_config(args.workload)
     from oracle.attention import attention_head
+    from oracle.attention_bwd import attention_bwd_query_rows
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     rows_per_step = 32
+    bwd = args.bwd_pass == "bwd"
 
     def step(i):
         b, h = heads[i % len(heads)]
         q, k, v = w.head_f64(b, h)
         rows = synth.sample_rows(q.shape[0], rows_per_step, w.seed + i, b, h)
+        if bwd:
+            do = synth.bf16_bits_to_f64(synth.make_grad_out(1, 1, w.N, w.d, seed=w.seed + i)[0, 0])
         t0 = time.perf_counter()
-        attention_head(q, k, v, w.causal, w.scale, rows=rows)
+        if bwd:
+            attention_bwd_query_rows(q, k, v, do, w.causal, w.scale, rows)
+        else:
+            attention_head(q, k, v, w.causal, w.scale, rows=rows)
         dt = time.perf_counter() - t0
         vis = (rows + 1) if w.causal else np.full(len(rows), w.N)
-        return dt, float(4.0 * w.d * vis.sum())
+        return dt, float(4.0 * w.d * vis.sum()) * (BWD_FLOP_RATIO if bwd else 1.0)
 
     for i in range(args.warmup):
         step(i)
@@ -237,10 +283,10 @@ def run_reference(args, world, rank):
         tot_t += dt
         tot_f += f
     value = tot_f / tot_t / 1e12
-    sample = (f"each step: {rows_per_step} seeded query rows of one head against all visible keys "
-              f"(fp64 numpy oracle, {_CORES} BLAS threads)")
+    sample = (f"each step: {'dq of ' if bwd else ''}{rows_per_step} seeded query rows of one head against all "
+              f"visible keys (fp64 numpy oracle, {_CORES} BLAS threads)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_block(args, w),
@@ -253,7 +299,8 @@ def run_reference(args, world, rank):
 def config_block(args, w):
     in_bytes = w.q.nbytes + w.k.nbytes + w.v.nbytes
     extra = {"Nq": int(w.q.shape[2]), "splits": args.splits} if w.name == "decode" else {}
-    return {"workload": f"{w.name}: {WORKLOAD_TEXT.get(w.name, '')}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+    what = "backward of " if getattr(args, "bwd_pass", "fwd") == "bwd" else ""
+    return {"workload": f"{what}{w.name}: {WORKLOAD_TEXT.get(w.name, '')}", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
             **extra,
             "causal": w.causal, "scale": w.scale, "seed": w.seed,
             "l2": (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB); no flush"
@@ -270,6 +317,8 @@ def main():
     ap.add_argument("--workload", default="cfg3", choices=sorted(synth.CONFIGS) + ["decode"])
     ap.add_argument("--splits", type=int, default=16, help="key-range splits of the decode workload")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pass", dest="bwd_pass", default="fwd", choices=["fwd", "bwd"],
+                    help="time the forward (default) or the backward of the workload")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -306,6 +355,9 @@ def main():
     else:
         w = synth.make_config(args.workload)
     fp8 = w.dtype == "e4m3"
+    bwd = args.bwd_pass == "bwd"
+    if bwd and (fp8 or decode):
+        raise SystemExit("--pass bwd runs on the bf16 square workloads (not the e4m3 one or decode)")
     if fp8:
         q_h, k_h, v_h = (torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (w.q, w.k, w.v))
         sc_h = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in (w.q_scale, w.k_scale, w.v_scale)]
@@ -319,13 +371,24 @@ def main():
     o = torch.empty((w.B, w.H, Nq, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, Nq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    flops = w.flops()
+    flops = w.flops() * (BWD_FLOP_RATIO if bwd else 1.0)
+    launches_per_step = 2 if decode else (3 if bwd else 1)
+    if bwd:
+        do_h = torch.from_numpy(synth.make_grad_out(w.B, w.H, w.N, w.d, seed=w.seed).view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+        dout = do_h.to(dev)
+        pkg.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        grads = [torch.empty_like(q) for _ in range(3)]
+        bws = torch.empty(pkg.bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
     if decode:
         ws = torch.empty(pkg.splitkv_workspace_bytes(w.B, w.H, Nq, w.d, args.splits), dtype=torch.uint8,
                          device=dev)
 
-    def forward(qq, kk, vv, ss):
-        if decode:
+    def forward(qq, kk, vv, ss, oo=None, dd=None, ll=None):
+        if bwd:
+            pkg.attn_bwd(qq, kk, vv, o if oo is None else oo, dout if dd is None else dd, lse if ll is None else ll,
+                         causal=w.causal, scale=w.scale, dq=grads[0], dk=grads[1], dv=grads[2], workspace=bws)
+        elif decode:
             pkg.attn_fwd_splitkv(qq, kk, vv, args.splits, causal=w.causal, scale=w.scale, o=o, lse=lse,
                                  workspace=ws)
         elif fp8:
@@ -333,7 +396,7 @@ def main():
         else:
             pkg.attn_fwd(qq, kk, vv, causal=w.causal, scale=w.scale, o=o, lse=lse)
 
-    in_bytes = q.nbytes + k.nbytes + v.nbytes
+    in_bytes = q.nbytes + k.nbytes + v.nbytes + ((o.nbytes + dout.nbytes) if bwd else 0)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if in_bytes <= L2_BYTES else None
 
     def step():
@@ -381,13 +444,22 @@ def main():
     value = job_throughput(flops, world, args.steps, total_ms)
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
 
-    # end to end through the public API: pinned host inputs -> device, forward,
-    # O and LSE back to pinned host memory, every step.
+    # end to end through the public API: pinned host inputs -> device, the pass,
+    # its results back to pinned host memory, every step.  Forward: Q, K, V in,
+    # O and LSE out.  Backward: Q, K, V, O, dO, LSE in, dQ, dK, dV out.
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
-    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     qd, kd, vd = (torch.empty_like(t) for t in (q, k, v))
     sd = [torch.empty_like(t) for t in scales]
+    if bwd:
+        o_in_h = o.cpu().pin_memory()
+        l_in_h = lse.cpu().pin_memory()
+        od, dd, ld = torch.empty_like(o), torch.empty_like(dout), torch.empty_like(lse)
+        outs = grads
+        in_host = [q_h, k_h, v_h, o_in_h, do_h, l_in_h]
+    else:
+        outs = [o, lse]
+        in_host = [q_h, k_h, v_h] + list(sc_h)
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
 
     def e2e_step():
         qd.copy_(q_h, non_blocking=True)
@@ -395,9 +467,15 @@ def main():
         vd.copy_(v_h, non_blocking=True)
         for dst, src in zip(sd, sc_h):
             dst.copy_(src, non_blocking=True)
-        forward(qd, kd, vd, sd)
-        o_h.copy_(o, non_blocking=True)
-        l_h.copy_(lse, non_blocking=True)
+        if bwd:
+            od.copy_(o_in_h, non_blocking=True)
+            dd.copy_(do_h, non_blocking=True)
+            ld.copy_(l_in_h, non_blocking=True)
+            forward(qd, kd, vd, sd, od, dd, ld)
+        else:
+            forward(qd, kd, vd, sd)
+        for dst, src in zip(outs_h, outs):
+            dst.copy_(src, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -420,10 +498,10 @@ def main():
     peak = float(peaks["bf16_tflops"]) * ratio
     src = (f"{peak_src} bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json)" if peak_src == "measured"
            else "fallback 1.9 PFLOP/s bf16") + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else "")
-    kname = {("bf16", 64): "attn_fwd_kernel<64,4,4,false>", ("bf16", 128): "attn_fwd_kernel<128,2,2,false>",
+    kname = "attn_bwd: prep + dq + dkdv kernels (whole step)" if bwd else {("bf16", 64): "attn_fwd_kernel<64,4,4,false>", ("bf16", 128): "attn_fwd_kernel<128,2,2,false>",
              ("e4m3", 128): "attn_fwd_kernel<128,3,3,true>"}.get((w.dtype, w.d), "attn_fwd_kernel")
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": traffic_for(w.name), "peak_source": src,
+            "traffic": traffic_for(w.name + (":bwd" if bwd else "")), "peak_source": src,
             "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * ratio),
             "kernel": kname, "avg_launch_ms": avg_kernel_ms, "flops_per_launch": flops}
     if fp8:
@@ -434,20 +512,20 @@ def main():
         roof["frac_of_mixed"] = achieved / mixed
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) inputs)",
         "config": config_block(args, w),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
-                "h2d_bytes_per_step": int(q_h.nbytes + k_h.nbytes + v_h.nbytes + sum(t.nbytes for t in sc_h)),
-                "d2h_bytes_per_step": int(o_h.nbytes + l_h.nbytes)},
-        "gpu_launches": args.steps,
+                "h2d_bytes_per_step": int(sum(t.nbytes for t in in_host)),
+                "d2h_bytes_per_step": int(sum(t.nbytes for t in outs_h))},
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        val, desc, secs = cpu_oracle_rate(w, args.cpu_budget)
+        val, desc, secs = (cpu_oracle_bwd_rate if bwd else cpu_oracle_rate)(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
                                 "sample": desc, "seconds": secs}
     if rank == 0:

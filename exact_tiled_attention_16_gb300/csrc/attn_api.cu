@@ -66,16 +66,17 @@ cudaError_t configure_kernel() {
 #define ATTN_BF16_D128 128, 2, 2, false   // 64 KB + 2 x 32 KB + 2 x 32 KB
 #define ATTN_FP8_D128 128, 3, 3, true     // 32 KB + 3 x 16 KB + 3 x 16 KB + 2 x 32 KB
 
-template <int D, int NS>
+template <int D, int RA, int RB>
 cudaError_t configure_bwd() {
-  const int bytes = static_cast<int>(BwdSmem<D, NS>::kBytes);
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const int bytes = static_cast<int>(BwdSmem<D, RA, RB>::kBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_bwd_dq_kernel<D, RA, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, RA, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
-// ring depth of the backward passes (two tiles per stage)
-constexpr int kBwdStagesD64 = 4;   // 32 KB + 4 x 32 KB
-constexpr int kBwdStagesD128 = 2;  // 64 KB + 2 x 64 KB
+// ring depths of the backward passes (ring A: K or Q, ring B: V or dO)
+#define ATTN_BWD_D64 64, 6, 4    // 2 + 10 tiles of 16 KB
+#define ATTN_BWD_D128 128, 3, 2  // 2 + 5 tiles of 32 KB
 
 // Per-device set-up on first use: architecture check, SM count, kernel
 // attributes, address of the error word.  Returns ATTN_OK or an error status.
@@ -101,7 +102,7 @@ int device_setup(int* dev_out) {
         configure_kernel<ATTN_BF16_D64, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, true>() != cudaSuccess ||
         configure_kernel<ATTN_FP8_D128, false>() != cudaSuccess ||
-        configure_bwd<64, kBwdStagesD64>() != cudaSuccess || configure_bwd<128, kBwdStagesD128>() != cudaSuccess ||
+        configure_bwd<ATTN_BWD_D64>() != cudaSuccess || configure_bwd<ATTN_BWD_D128>() != cudaSuccess ||
         cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_ptr), g_attn_err) != cudaSuccess) {
       st.status = ATTN_ERR_CUDA;
       return;
@@ -237,21 +238,21 @@ size_t splitkv_workspace_bytes(long long BH, long long Nq, long long d, long lon
 }  // namespace
 
 namespace {
-template <int D, int NS>
+template <int D, int RA, int RB>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                const BwdParams& bp, int dev, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const long long rows = static_cast<long long>(bp.BH) * bp.N;
+  const long long rows = static_cast<long long>(bp.BH) * bp.Npad;
   long long pblocks = (rows + 7) / 8;
   const long long cap = static_cast<long long>(g_dev[dev].num_sms) * 8;
   if (pblocks > cap) pblocks = cap;
   attn_bwd_prep_kernel<D><<<static_cast<int>(pblocks), 256, 0, st>>>(bp);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   const int grid = bp.num_units < g_dev[dev].num_sms ? bp.num_units : g_dev[dev].num_sms;
-  const size_t smem = BwdSmem<D, NS>::kBytes;
-  attn_bwd_dq_kernel<D, NS><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
+  const size_t smem = BwdSmem<D, RA, RB>::kBytes;
+  attn_bwd_dq_kernel<D, RA, RB><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-  attn_bwd_dkdv_kernel<D, NS><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
+  attn_bwd_dkdv_kernel<D, RA, RB><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 }  // namespace
@@ -373,7 +374,9 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N) {
   if (B < 1 || H < 1 || N < 1) return 0;
-  return static_cast<size_t>(B) * H * N * sizeof(float);  // D_i = do_i . o_i
+  // two float arrays [B*H][N rounded up to 128]: -lse log2e and -scale D_i
+  const size_t npad = (static_cast<size_t>(N) + kBlockM - 1) / kBlockM * kBlockM;
+  return 2 * static_cast<size_t>(B) * H * npad * sizeof(float);
 }
 
 
@@ -386,7 +389,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if ((reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
        reinterpret_cast<uintptr_t>(dv)) & 15u)
     return ATTN_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(workspace)) & 3u) return ATTN_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_ALIGN;
   if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N)) return ATTN_ERR_DIMS;
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
@@ -401,21 +405,23 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   bp.o = static_cast<const __nv_bfloat16*>(o);
   bp.dout = static_cast<const __nv_bfloat16*>(dout);
   bp.lse = lse;
-  bp.dvec = static_cast<float*>(workspace);
+  bp.num_blocks = (N + kBlockN - 1) / kBlockN;
+  bp.Npad = bp.num_blocks * kBlockN;
+  bp.nlse2 = static_cast<float*>(workspace);
+  bp.nds = bp.nlse2 + static_cast<size_t>(B) * H * bp.Npad;
   bp.dq = static_cast<__nv_bfloat16*>(dq);
   bp.dk = static_cast<__nv_bfloat16*>(dk);
   bp.dv = static_cast<__nv_bfloat16*>(dv);
   bp.BH = BH;
   bp.N = N;
-  bp.num_blocks = (N + kBlockN - 1) / kBlockN;
   bp.num_units = BH * bp.num_blocks;
   bp.causal = causal ? 1 : 0;
   bp.scale = scale;
   bp.scale_log2 = scale * 1.4426950408889634f;
   bp.timeout_ns = g_timeout_ns;
   bp.err = g_dev[dev].err_ptr;
-  if (d == 64) return launch_bwd<64, kBwdStagesD64>(mq, mk, mv, mdo, bp, dev, stream);
-  return launch_bwd<128, kBwdStagesD128>(mq, mk, mv, mdo, bp, dev, stream);
+  if (d == 64) return launch_bwd<ATTN_BWD_D64>(mq, mk, mv, mdo, bp, dev, stream);
+  return launch_bwd<ATTN_BWD_D128>(mq, mk, mv, mdo, bp, dev, stream);
 }
 
 const char* attn_status_string(int status) {

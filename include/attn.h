@@ -181,7 +181,8 @@ size_t attn_splitkv_static_scratch_bytes(void);
  *   lse              : const float32 [B,H,N]
  *   dq, dk, dv       : bf16 [B,H,N,d] outputs, 16-byte aligned
  *   workspace        : device scratch of at least attn_bwd_workspace_bytes(B,H,N)
- *                      bytes (4-byte aligned), owned by the caller
+ *                      bytes (16-byte aligned), owned by the caller; the call
+ *                      overwrites it
  *   d : 64 or 128; other arguments as attn_fwd.  Deterministic (no atomics).
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

@@ -122,7 +122,7 @@ def test_partial_merge_splitkv_validation(lib):
 def test_bwd_validation(lib):
     import exact_tiled_attention_16_gb300._lib as L
     a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, dout=0x5000, lse=0x6000, dq=0x7000, dk=0x8000, dv=0x9000,
-             B=1, H=2, N=100, d=64, causal=1, scale=0.125, workspace=0xa000, workspace_bytes=800)
+             B=1, H=2, N=100, d=64, causal=1, scale=0.125, workspace=0xa000, workspace_bytes=2048)
 
     def call(**kw):
         x = dict(a)
@@ -138,8 +138,11 @@ def test_bwd_validation(lib):
     assert call(dout=0x5008) == -5
     assert call(dk=0x8002) == -5
     assert call(lse=0x6002) == -5
-    assert call(workspace_bytes=799) == -2  # D vector: B*H*N floats
-    assert L.bwd_workspace_bytes(1, 2, 100) == 800
+    assert call(workspace=0xa008) == -5
+    # two float arrays of B*H rows of N rounded up to 128
+    assert call(workspace_bytes=2047) == -2
+    assert L.bwd_workspace_bytes(1, 2, 100) == 2 * 2 * 128 * 4
+    assert L.bwd_workspace_bytes(2, 3, 257) == 2 * 6 * 384 * 4
     assert L.bwd_workspace_bytes(0, 2, 100) == 0
 
 

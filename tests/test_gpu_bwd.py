@@ -166,9 +166,10 @@ def test_no_writes_outside_outputs():
     guard, n = 4096, B * H * N * d
     bufs = [torch.full((n + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
     views = [b[guard:guard + n].view(B, H, N, d) for b in bufs]
-    ws = torch.full((B * H * N + 2 * 1024,), float("nan"), dtype=torch.float32, device="cuda")
+    nws = pkg.bwd_workspace_bytes(B, H, N) // 4
+    ws = torch.full((nws + 2 * 1024,), float("nan"), dtype=torch.float32, device="cuda")
     pkg.attn_bwd(q, k, v, o, do, lse, scale=w.scale, dq=views[0], dk=views[1], dv=views[2],
-                 workspace=ws[1024:1024 + B * H * N])
+                 workspace=ws[1024:1024 + nws])
     torch.cuda.synchronize()
     for b in bufs:
         assert torch.isnan(b[:guard].float()).all() and torch.isnan(b[-guard:].float()).all()
