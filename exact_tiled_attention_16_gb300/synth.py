@@ -148,6 +148,80 @@ def block_dequantize_e4m3(codes: np.ndarray, scales: np.ndarray, block: int = FP
 
 
 # ----------------------------------------------------------------------------
+# OCP FP4 E2M1 with MX block scaling (MXFP4): element codes are 1 sign bit,
+# 2 exponent bits (bias 1) and 1 mantissa bit, magnitudes {0, 0.5, 1, 1.5, 2,
+# 3, 4, 6} for codes 0..7 (exponent field 0: subnormal m * 0.5); no infinities
+# or NaNs.  A block of 32 elements shares one E8M0 scale (an unsigned biased
+# exponent, value 2^(byte - 127), byte 255 reserved for NaN); the shared
+# exponent is floor(log2(amax)) - 2, 2 being the largest element exponent.
+# Two codes share a byte, the even-indexed element in the low nibble.
+# ----------------------------------------------------------------------------
+E2M1_MAX = 6.0
+MX_BLOCK = 32
+_E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    """4-bit codes (0..15, one per array element) -> float64 values."""
+    c = np.asarray(codes).astype(np.int64)
+    mag = _E2M1_POS[c & 7]
+    return np.where((c & 8) != 0, -mag, mag)
+
+
+def e2m1_encode_satfinite(x: np.ndarray) -> np.ndarray:
+    """float -> 4-bit e2m1 code (uint8 0..15), round to nearest, ties to the
+    even code, saturating to +-6; negative inputs keep the sign bit."""
+    xf = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(xf), E2M1_MAX)
+    hi = np.minimum(np.searchsorted(_E2M1_POS, a, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    dlo = a - _E2M1_POS[lo]
+    dhi = _E2M1_POS[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(_E2M1_POS[hi] == a, hi, code)
+    return (code.astype(np.uint8) | (np.signbit(xf).astype(np.uint8) << np.uint8(3))).astype(np.uint8)
+
+
+def mx_shared_exponent(amax: np.ndarray) -> np.ndarray:
+    """E8M0 shared exponent of MXFP4 blocks: floor(log2(amax)) - 2, clamped to
+    [-127, 127]; -127 for an all-zero block."""
+    a = np.asarray(amax, dtype=np.float64)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))  # a = f * 2^e, f in [0.5, 1)
+    ex = (e - 1) - 2
+    return np.where(a > 0, np.clip(ex, -127, 127), -127).astype(np.int64)
+
+
+def mxfp4_quantize_keys(v: np.ndarray):
+    """MXFP4 quantisation of V [B,H,N,d] along the key axis, stored transposed.
+
+    For every (b, h, channel c, block of 32 consecutive keys): X = 2^E with E =
+    mx_shared_exponent(amax of the block), codes = e2m1_RNE_satfinite(v / X).
+    Returns (packed codes uint8 [B,H,d,N/2] -- key 2i in the low nibble of byte
+    i --, scale bytes uint8 [B,H,d,N/32] = E + 127).  N must be a multiple of 32."""
+    B, H, N, d = v.shape
+    assert N % MX_BLOCK == 0
+    vt = np.asarray(v, dtype=np.float64).transpose(0, 1, 3, 2)  # [B,H,d,N]
+    blocks = vt.reshape(B, H, d, N // MX_BLOCK, MX_BLOCK)
+    e = mx_shared_exponent(np.abs(blocks).max(axis=4))
+    codes = e2m1_encode_satfinite(blocks / np.ldexp(1.0, e)[..., None]).reshape(B, H, d, N)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << np.uint8(4))).astype(np.uint8)
+    return np.ascontiguousarray(packed), (e + 127).astype(np.uint8)
+
+
+def mxfp4_dequantize_keys(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """(packed [B,H,d,N/2], scale bytes [B,H,d,N/32]) -> V [B,H,N,d] float64."""
+    B, H, d, half = packed.shape
+    N = 2 * half
+    codes = np.empty((B, H, d, N), dtype=np.uint8)
+    codes[..., 0::2] = packed & np.uint8(15)
+    codes[..., 1::2] = packed >> np.uint8(4)
+    x = np.ldexp(1.0, scales.astype(np.int64) - 127)
+    vals = e2m1_decode(codes).reshape(B, H, d, N // MX_BLOCK, MX_BLOCK) * x[..., None]
+    return vals.reshape(B, H, d, N).transpose(0, 1, 3, 2)
+
+
+# ----------------------------------------------------------------------------
 # Outlier channels and the random orthogonal rotation
 # ----------------------------------------------------------------------------
 
@@ -211,6 +285,10 @@ class Workload:
         if self.dtype == "bf16":
             return (bf16_bits_to_f64(self.q[b, h]), bf16_bits_to_f64(self.k[b, h]),
                     bf16_bits_to_f64(self.v[b, h]))
+        if self.dtype == "e4m3_e2m1":
+            return (block_dequantize_e4m3(self.q[b:b + 1, h:h + 1], self.q_scale[b:b + 1, h:h + 1])[0, 0],
+                    block_dequantize_e4m3(self.k[b:b + 1, h:h + 1], self.k_scale[b:b + 1, h:h + 1])[0, 0],
+                    mxfp4_dequantize_keys(self.v[b:b + 1, h:h + 1], self.v_scale[b:b + 1, h:h + 1])[0, 0])
         return (block_dequantize_e4m3(self.q[b:b + 1, h:h + 1], self.q_scale[b:b + 1, h:h + 1])[0, 0],
                 block_dequantize_e4m3(self.k[b:b + 1, h:h + 1], self.k_scale[b:b + 1, h:h + 1])[0, 0],
                 block_dequantize_e4m3(self.v[b:b + 1, h:h + 1], self.v_scale[b:b + 1, h:h + 1])[0, 0])
@@ -275,6 +353,22 @@ def make_fp8(B, H, N, d, causal, seed, scale=None, outlier_frac=0.01, outlier_mu
         scale = 1.0 / math.sqrt(d)
     return Workload(name, "e4m3", B, H, N, d, bool(causal), float(scale), seed, q8, k8, v8,
                     qs, ks, vs, meta=meta)
+
+
+def make_fp4p(B, H, N, d, causal, seed, scale=None, outlier_frac=0.01, outlier_mult=10.0,
+              rotate=True, name="e4m3_e2m1") -> Workload:
+    """Workload of the Direct-P FP4 path: Q and K exactly as make_fp8 draws and
+    quantises them (e4m3, per-128-token scales); V from the same draw (with its
+    outlier channels) quantised to MXFP4 along the keys and stored transposed:
+    w.v = packed codes [B,H,d,N/2], w.v_scale = E8M0 bytes [B,H,d,N/32]."""
+    w8 = make_fp8(B, H, N, d, causal, seed, scale, outlier_frac, outlier_mult, rotate, name)
+    v = normal_f32((B, H, N, d), seed, STREAM_V).astype(np.float64)
+    if outlier_frac > 0:
+        v[..., outlier_channels(d, outlier_frac, seed, STREAM_OUTLIER_V)] *= outlier_mult
+    vt, vts = mxfp4_quantize_keys(v)
+    w8.dtype = "e4m3_e2m1"
+    w8.v, w8.v_scale = vt, vts
+    return w8
 
 
 # The five workload shapes (seeded; the FlashAttention pages quote no dataset).

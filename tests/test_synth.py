@@ -151,3 +151,65 @@ def test_flop_count_convention():
     w = synth.make_bf16(1, 1, 8, 4, True, 0)
     assert w.flops() == 4 * 8 * 8 * 4 / 2
     assert math.isclose(synth.make_bf16(1, 1, 8, 4, False, 0).flops(), 4 * 8 * 8 * 4)
+
+
+# --------------------------------------------------------------------- MXFP4
+def test_e2m1_decode_table_from_the_format():
+    """Codes decode by the E2M1 definition: sign bit 3, exponent bits 2-1 (bias
+    1), mantissa bit 0; exponent field 0 is subnormal (m * 0.5)."""
+    for code in range(16):
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        mag = m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1)
+        assert synth.e2m1_decode(np.array([code]))[0] == (-mag if s else mag)
+
+
+def test_e2m1_encode_rounding_and_saturation():
+    vals = synth.e2m1_decode(np.arange(8))
+    # every representable value encodes to itself, either sign
+    np.testing.assert_array_equal(synth.e2m1_encode_satfinite(vals), np.arange(8))
+    np.testing.assert_array_equal(synth.e2m1_encode_satfinite(-vals[1:]), np.arange(1, 8) | 8)
+    # midpoints go to the even code; values past 6 saturate
+    mids = (vals[:-1] + vals[1:]) / 2
+    np.testing.assert_array_equal(synth.e2m1_encode_satfinite(mids), [0, 2, 2, 4, 4, 6, 6])
+    np.testing.assert_array_equal(synth.e2m1_encode_satfinite(np.array([6.01, 1e9])), [7, 7])
+    # nearest otherwise: brute force over a grid
+    g = np.linspace(0, 6, 6001)
+    nearest = np.abs(g[:, None] - vals[None, :]).min(axis=1)
+    got = np.abs(synth.e2m1_decode(synth.e2m1_encode_satfinite(g)) - g)
+    np.testing.assert_allclose(got, nearest, atol=0)
+
+
+def test_mx_shared_exponent_definition():
+    """E = floor(log2 amax) - 2: amax / 2^E lies in [4, 8); all-zero blocks -127."""
+    a = np.exp2(np.random.default_rng(0).uniform(-60, 60, size=10000))
+    e = synth.mx_shared_exponent(a)
+    r = a / np.exp2(e.astype(float))
+    assert (r >= 4).all() and (r < 8).all()
+    assert synth.mx_shared_exponent(np.array([0.0]))[0] == -127
+    assert synth.mx_shared_exponent(np.array([1.0, 4.0, 7.99]))[2] == 0
+
+
+def test_mxfp4_layout_round_trip_and_error_bound():
+    g = np.random.default_rng(1)
+    B, H, N, d = 2, 3, 96, 8
+    # representable blocks survive exactly: values e2m1 * 2^E with one element at 4 * 2^E
+    e = g.integers(-10, 10, size=(B, H, d, N // 32))
+    codes = g.integers(0, 16, size=(B, H, d, N))
+    codes[..., ::32] = 6
+    x = synth.e2m1_decode(codes) * np.repeat(np.exp2(e.astype(float)), 32, axis=3)
+    v = x.transpose(0, 1, 3, 2)  # [B,H,N,d]
+    packed, sc = synth.mxfp4_quantize_keys(v)
+    assert packed.shape == (B, H, d, N // 2) and sc.shape == (B, H, d, N // 32)
+    np.testing.assert_array_equal(synth.mxfp4_dequantize_keys(packed, sc), v)
+    np.testing.assert_array_equal(sc.astype(int) - 127, e)
+    # nibble order: key 2i in the low nibble of byte i
+    assert (packed[0, 0, 0, 0] & 15) == (synth.e2m1_encode_satfinite(v[0, 0, 0, 0] / 2.0 ** e[0, 0, 0, 0]))
+    # arbitrary data: error at most half an e2m1 step, or the saturation at 6 X
+    w = g.standard_normal((B, H, N, d)) * 3
+    packed, sc = synth.mxfp4_quantize_keys(w)
+    back = synth.mxfp4_dequantize_keys(packed, sc)
+    X = np.repeat(np.exp2(sc.astype(float) - 127), 32, axis=3).transpose(0, 1, 3, 2)
+    y = np.abs(w) / X
+    half_step = np.where(y < 2, 0.25, np.where(y < 4, 0.5, 1.0))
+    allowed = np.where(y > 6, y - 6, half_step) * X
+    assert (np.abs(back - w) <= allowed + 1e-12).all()
