@@ -40,6 +40,8 @@ def load_library():
     lib.attn_fwd.restype = ci
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
     lib.attn_fwd_fp8.restype = ci
+    lib.attn_fwd_fp4p.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
+    lib.attn_fwd_fp4p.restype = ci
     lib.attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, vp]
     lib.attn_fwd_partial.restype = ci
     lib.attn_merge.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ci, vp, vp, ci, ci, ci, ci, ci, vp]
@@ -147,6 +149,41 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sc
                           B, H, N, d, causal, scale, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8")
+    return o, lse
+
+
+def attn_fwd_fp4p_raw(q8: int, k8: int, vt4: int, q_scale: int, k_scale: int, vt_scale: int, o: int, lse: int,
+                      B: int, H: int, N: int, d: int, causal: bool, scale: float, stream: int) -> int:
+    return load_library().attn_fwd_fp4p(q8 or None, k8 or None, vt4 or None, q_scale or None, k_scale or None,
+                                        vt_scale or None, o or None, lse or None, B, H, N, d, 1 if causal else 0,
+                                        float(scale), stream or None)
+
+
+def attn_fwd_fp4p(q8, k8, vt4, q_scale, k_scale, vt_scale, causal: bool = False, scale: float | None = None,
+                  o=None, lse=None, want_lse: bool = True, stream=None):
+    """Direct-P FP4 attention forward.  q8, k8: uint8 e4m3 codes [B,H,N,d] with
+    fp32 block scales [B,H,N/128]; vt4: uint8 MXFP4 codes of V^T [B,H,d,N/2];
+    vt_scale: uint8 E8M0 scales [B,H,d,N/32].  Returns (o bf16, lse fp32)."""
+    import torch
+    for name, t, dt in (("q8", q8, torch.uint8), ("k8", k8, torch.uint8), ("vt4", vt4, torch.uint8),
+                        ("q_scale", q_scale, torch.float32), ("k_scale", k_scale, torch.float32),
+                        ("vt_scale", vt_scale, torch.uint8)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or vt4.shape != (B, H, d, N // 2) or vt_scale.shape != (B, H, d, N // 32):
+        raise ValueError("shapes: q8, k8 [B,H,N,d]; vt4 [B,H,d,N/2]; vt_scale [B,H,d,N/32]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    rc = attn_fwd_fp4p_raw(q8.data_ptr(), k8.data_ptr(), vt4.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
+                           vt_scale.data_ptr(), o.data_ptr(), lse.data_ptr() if lse is not None else 0, B, H, N, d,
+                           causal, scale, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp4p")
     return o, lse
 
 

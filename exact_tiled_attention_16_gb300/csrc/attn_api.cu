@@ -53,11 +53,11 @@ EncodeTiledFn get_encode() {
   return g_encode;
 }
 
-template <int D, int NK, int NV, bool kFp8, bool kPartial>
+template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false>
 cudaError_t configure_kernel() {
-  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8, kPartial>,
+  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(SmemPlan<D, NK, NV, kFp8>::kBytes));
+                              static_cast<int>(SmemPlan<D, NK, NV, kFp8, kFp4>::kBytes));
 }
 
 // Ring depths (K stages, V stages) per instance; shared memory holds the two Q
@@ -65,6 +65,7 @@ cudaError_t configure_kernel() {
 #define ATTN_BF16_D64 64, 4, 4, false     // 32 KB + 4 x 16 KB + 4 x 16 KB
 #define ATTN_BF16_D128 128, 2, 2, false   // 64 KB + 2 x 32 KB + 2 x 32 KB
 #define ATTN_FP8_D128 128, 3, 3, true     // 32 KB + 3 x 16 KB + 3 x 16 KB + 2 x 32 KB
+#define ATTN_FP4_D128 128, 4, 4, true     // Direct-P FP4: 32 KB + 4 x 16 KB + 4 x 8 KB (V^T e2m1)
 
 template <int D, int RA, int RB>
 cudaError_t configure_bwd() {
@@ -102,6 +103,7 @@ int device_setup(int* dev_out) {
         configure_kernel<ATTN_BF16_D64, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, true>() != cudaSuccess ||
         configure_kernel<ATTN_FP8_D128, false>() != cudaSuccess ||
+        configure_kernel<ATTN_FP4_D128, false, true>() != cudaSuccess ||
         configure_bwd<ATTN_BWD_D64>() != cudaSuccess || configure_bwd<ATTN_BWD_D128>() != cudaSuccess ||
         cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_ptr), g_attn_err) != cudaSuccess) {
       st.status = ATTN_ERR_CUDA;
@@ -126,6 +128,22 @@ int make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, uint32_t
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_OVERFLOW;
+}
+
+// V^T of the Direct-P FP4 path: packed e2m1 bytes [BH][d][N/2] viewed as 3-D
+// (N/2, d, BH); box = 64 bytes (128 keys) x d rows, 64-byte swizzle.
+int make_map_vt4(CUtensorMap* map, const void* ptr, int d, int N, int BH) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return ATTN_ERR_CUDA;
+  const cuuint64_t row = static_cast<cuuint64_t>(N) / 2;
+  cuuint64_t dims[3] = {row, static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {row, row * static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(d), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_OVERFLOW;
 }
@@ -177,14 +195,15 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
   p.err = g_dev[dev].err_ptr;
 }
 
-template <int D, int NK, int NV, bool kFp8, bool kPartial>
+template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p, int dev,
            void* stream) {
   // work items dealt to CTAs: units, or combined heavy+light pairs under zigzag
   const int items = p.zigzag ? p.BH * ((p.num_pairs + 1) / 2) : p.num_units;
   const int grid = items < g_dev[dev].num_sms ? items : g_dev[dev].num_sms;
-  attn_fwd_kernel<D, NK, NV, kFp8, kPartial><<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8>::kBytes,
-                                               static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, p);
+  attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4>
+      <<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8, kFp4>::kBytes, static_cast<cudaStream_t>(stream)>>>(mq, mk,
+                                                                                                        mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -298,6 +317,36 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   return launch<ATTN_FP8_D128, false>(mq, mk, mv, p, dev, stream);
+}
+
+int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* q_scale, const float* k_scale,
+                  const uint8_t* vt_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                  void* stream) {
+  int rc = validate_tensors(q8, k8, vt4, o, lse, B, H, N, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  if (N % kBlockN != 0) return ATTN_ERR_DIMS;
+  // the kernel indexes the scale words of V^T with 32-bit integers
+  if (static_cast<long long>(B) * H * d * (N / kBlockN) >= (1ll << 32)) return ATTN_ERR_OVERFLOW;
+  if (!q_scale || !k_scale || !vt_scale) return ATTN_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(vt_scale)) & 3u)
+    return ATTN_ERR_ALIGN;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
+  if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
+  if ((rc = make_map_vt4(&mv, vt4, d, N, BH)) != ATTN_OK) return rc;
+  FwdParams p;
+  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = reinterpret_cast<const float*>(vt_scale);  // E8M0 words, read as such by the FP4 path
+  return launch<ATTN_FP4_D128, false, true>(mq, mk, mv, p, dev, stream);
 }
 
 int attn_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,

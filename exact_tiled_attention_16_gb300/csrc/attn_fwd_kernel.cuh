@@ -51,6 +51,19 @@
 // outlier channels).  The V block scale and a 2^6 pre-scale are folded into the
 // exponent offset, P' = 2^(x - m + 6 + log2(s_v[j] / max s_v)) <= 2^14, and at
 // the end O = O' * max s_v / (64 l).
+//
+// Direct-P FP4 variant (kFp4, with kFp8's e4m3 Q K^T): P V runs on the FP4
+// tensor cores (kind::mxf4: e2m1 elements, one power-of-two scale per 32 keys),
+// with V supplied as MXFP4 along the keys and stored transposed ([d][N/2] bytes,
+// K-major, 64-byte swizzle).  P goes from scores to 4-bit codes directly (the
+// FP4 FlashAttention-4 summary's Direct-P): each 32-key block of a row takes its
+// scale exponent E from its largest score, E = ceil(max t), so the code of a key
+// is e2m1(2^(t - E + 2)) -- one exponential and one conversion, no pass over the
+// probabilities to find their block maximum and no division by the scale.  The
+// running max moves in whole powers of two, so rescales are exact and the codes
+// depend on the scores alone.  P (16 columns), its scales and V's scales are
+// written into dead S_t columns (0..15, 32..35, 64..67); the row sum is taken
+// from the codes.
 #pragma once
 
 #include <cuda.h>
@@ -81,6 +94,8 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kRegsLaunch * kNumT
 // at most 2^8, which the 16-bit P and the fp32 accumulators absorb.
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kFp8PScaleLog2 = 6.0f;
+// Direct-P FP4: TMEM columns (within S_t) of the P scales and the V^T scales
+constexpr uint32_t kFp4SfaCol = 32, kFp4SfbCol = 64;
 
 struct FwdParams {
   __nv_bfloat16* o;   // final output: [B*H, Nq, D] bf16
@@ -101,7 +116,8 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e)
   const float* q_scale;  // FP8 only: [B*H, num_kblocks] block scales
   const float* k_scale;
-  const float* v_scale;
+  const float* v_scale;  // FP8; the Direct-P FP4 path keeps here the E8M0 scales of
+                         //   V^T, 32-bit words of four bytes: [B*H, D, Nk/128]
   unsigned long long timeout_ns;
   int* err;           // device error word (first failure wins)
 };
@@ -120,15 +136,17 @@ struct TileLayout {
 
 // Shared-memory plan of one instance: Q tiles, K ring, V ring and (FP8) the f16
 // copy of V, then the mbarriers.
-template <int D, int NK, int NV, bool kFp8>
+template <int D, int NK, int NV, bool kFp8, bool kFp4 = false>
 struct SmemPlan {
   using In = TileLayout<D, kFp8 ? 1 : 2>;   // Q, K, V as loaded
   using V16 = TileLayout<D, 2>;              // V operand of P V (bf16 or f16)
-  static constexpr int kNumConv = kFp8 ? 2 : 0;
+  static constexpr int kNumConv = (kFp8 && !kFp4) ? 2 : 0;
+  // FP4: a V^T tile is D rows of 128 keys x 4 bits = 64 bytes
+  static constexpr uint32_t kVTileBytes = kFp4 ? D * 64 : In::kTileBytes;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kTilesPerUnit * In::kTileBytes;
   static constexpr uint32_t kV = kK + NK * In::kTileBytes;
-  static constexpr uint32_t kC = kV + NV * In::kTileBytes;
+  static constexpr uint32_t kC = kV + NV * kVTileBytes;
   static constexpr uint32_t kBars = kC + kNumConv * V16::kTileBytes;
   static constexpr int kNumBars = 12 + 2 * NK + 2 * NV + 2 * kNumConv;
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBars + 8 * kNumBars + 16;
@@ -224,11 +242,12 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // kPartial selects the output: false = normalised bf16 O and lse (every query
 // row sees key 0: no position offsets, no splits); true = per-split fp32 O and
 // lse, where a tile or row may see no key at all.
-template <int D, int NK, int NV, bool kFp8, bool kPartial>
+template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
-  using Plan = SmemPlan<D, NK, NV, kFp8>;
+  static_assert(!kFp4 || (kFp8 && D == 128 && !kPartial), "Direct-P FP4: e4m3 Q K^T, d = 128, final output");
+  using Plan = SmemPlan<D, NK, NV, kFp8, kFp4>;
   using L = typename Plan::In;
   using LV = typename Plan::V16;
   constexpr uint32_t kTmemS[2] = {0, 128};
@@ -281,7 +300,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(b_v_full + 8 * s, 1);
-      mbar_init(b_v_empty + 8 * s, kFp8 ? kConvertThreads : 1);
+      mbar_init(b_v_empty + 8 * s, Plan::kNumConv > 0 ? kConvertThreads : 1);
     }
     for (int b = 0; b < Plan::kNumConv; ++b) {
       mbar_init(b_c_full + 8 * b, kConvertThreads);
@@ -338,10 +357,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           ++gk;
           const uint32_t sv = gv % NV, uv = gv / NV;
           if (uv > 0 && !(ok = mbar_wait(b_v_empty + 8 * sv, (uv - 1) & 1, abort_flag, tmo, p.err, 3))) break;
-          mbar_arrive_expect_tx(b_v_full + 8 * sv, L::kTileBytes);
-          for (int c = 0; c < (int)L::kChunks; ++c)
-            tma_load_3d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tmap_v, b_v_full + 8 * sv,
-                        c * L::kChunkElems, key0, ui.bh, pol_kv);
+          mbar_arrive_expect_tx(b_v_full + 8 * sv, Plan::kVTileBytes);
+          if constexpr (kFp4) {
+            // V^T: the block's 64 bytes of keys in every one of the D rows
+            tma_load_3d(sV + sv * Plan::kVTileBytes, &tmap_v, b_v_full + 8 * sv, key0 / 2, 0, ui.bh, pol_kv);
+          } else {
+            for (int c = 0; c < (int)L::kChunks; ++c)
+              tma_load_3d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tmap_v, b_v_full + 8 * sv,
+                          c * L::kChunkElems, key0, ui.bh, pol_kv);
+          }
           ++gv;
         }
         ++units;
@@ -393,11 +417,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       // per column), V MN-major, 16 key rows of 128 bytes per step, column chunks
       // kChunkBytes apart.
       auto issue_pv = [&](int t, uint32_t v_base, bool accumulate) {
+        if constexpr (kFp4) {
+          // P_t (e2m1, S_t columns 0..15) x V^T (K-major, 64-byte swizzle): two
+          // K = 64 steps of 32 bytes; scale words of P and V in S_t's columns too
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_f16_ts(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8,
-                     sdesc_sw128(v_base + kk * 16 * 128, LV::kChunkBytes, 1024), idesc_o,
-                     (accumulate || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 2; ++kk)
+            mma_mxf4_ts(tmem + kTmemO[t], tmem + kTmemS[t] + 8 * kk, sdesc_sw64(v_base + 32 * kk, 512),
+                        make_idesc_mxf4(kBlockM, D, 2 * kk), tmem + kTmemS[t] + kFp4SfaCol,
+                        tmem + kTmemS[t] + kFp4SfbCol, (accumulate || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk)
+            mma_f16_ts(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8,
+                       sdesc_sw128(v_base + kk * 16 * 128, LV::kChunkBytes, 1024), idesc_o,
+                       (accumulate || kk > 0) ? 1u : 0u);
+        }
       };
       int o_uses[2] = {0, 0};  // units in which tile t has written O_t
       for (int round = 0; ok; ++round) {
@@ -422,7 +456,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           const uint32_t skn = (gj + 1) % NK, phkn = ((gj + 1) / NK) & 1;
           // the 16-bit V operand of block j
           uint32_t v_base, v_bar, v_par;
-          if constexpr (kFp8) {
+          if constexpr (kFp4) {
+            v_base = sV + (gj % NV) * Plan::kVTileBytes;
+            v_bar = b_v_full + 8 * (gj % NV);
+            v_par = (gj / NV) & 1;
+          } else if constexpr (kFp8) {
             v_base = sC + (gj & 1) * LV::kTileBytes;
             v_bar = b_c_full + 8 * (gj & 1);
             v_par = (gj >> 1) & 1;
@@ -449,7 +487,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (j == nt - 1) mma_commit(b_pv_done + 8 * t);
             if (t == 1) {
               // tile 1 is the last user of V_j
-              if constexpr (kFp8) mma_commit(b_c_empty + 8 * (gj & 1));
+              if constexpr (Plan::kNumConv > 0) mma_commit(b_c_empty + 8 * (gj & 1));
               else mma_commit(b_v_empty + 8 * (gj % NV));
             }
             if (j + 1 < nt) {
@@ -470,7 +508,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       mma_commit(b_drain);
       volatile int no_abort = 0;
       mbar_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
-    } else if (kFp8 && warp >= kConvertWarp0) {
+    } else if (Plan::kNumConv > 0 && warp >= kConvertWarp0) {
       // ------------------------------------------------- FP8: V e4m3 -> f16
       // Each thread converts 16 of the 1024 16-byte units of a V block (128 key
       // rows x 128 e4m3): the 16 codes of a unit become 32 bytes of f16 in the
@@ -544,7 +582,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       float sv_max = 1.f;
       const float* ks_row = nullptr;
       const float* vs_row = nullptr;
-      if constexpr (kFp8) {
+      if constexpr (kFp4) {
+        const size_t sb = static_cast<size_t>(bh) * p.num_kblocks;
+        ks_row = p.k_scale + sb;
+        c_q *= __ldg(p.q_scale + sb + (qt < p.num_kblocks ? qt : p.num_kblocks - 1));
+      } else if constexpr (kFp8) {
         const size_t sb = static_cast<size_t>(bh) * p.num_kblocks;
         ks_row = p.k_scale + sb;
         vs_row = p.v_scale + sb;
@@ -552,13 +594,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         sv_max = 0.f;  // largest V block scale this tile uses (scales are > 0)
         for (int jj = 0; jj < nkv; ++jj) sv_max = fmaxf(sv_max, __ldg(vs_row + ui.kb0 + jj));
       }
+      // FP4: the V^T scale words this lane supplies, channel rows lane, lane + 32, ...
+      // (word index into p.vt_scale; the launch checks that it fits 32 bits)
+      uint32_t vts_idx = 0, vts_stride = 0;
+      if constexpr (kFp4) {
+        vts_stride = static_cast<uint32_t>(p.Nk / kBlockN);
+        vts_idx = (static_cast<uint32_t>(bh) * D + (threadIdx.x & 31)) * vts_stride;
+      }
       float m_use = -INFINITY;  // running max in log2 units (scale folded in)
       float l = 0.f;            // running normaliser against m_use
       for (int j = 0; j < nkv; ++j) {
         const int jb = ui.kb0 + j;  // K/V block index
         float cj = c_q;
         float off = 0.f;  // FP8: log2 of the pre-scale and V block-scale ratio
-        if constexpr (kFp8) {
+        if constexpr (kFp4) {
+          cj *= __ldg(ks_row + jb);
+        } else if constexpr (kFp8) {
           cj *= __ldg(ks_row + jb);
           off = kFp8PScaleLog2 + lg2_approx(__ldg(vs_row + jb) / sv_max);
         }
@@ -581,55 +632,141 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           for (int c = 0; c < kBlockN; ++c)
             if (c > lim) s[c] = -INFINITY;
         }
-        // row max: four independent chains of three-input max
-        float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+        if constexpr (kFp4) {
+          // Direct-P.  Block maxima of the raw scores (cj > 0 keeps the order)
+          float bm[4];
 #pragma unroll
-        for (int c = 4; c < kBlockN; c += 8) {
-          a0 = fmax3(a0, s[c], s[c + 1]);
-          a1 = fmax3(a1, s[c + 2], s[c + 3]);
-          a2 = fmax3(a2, s[c + 4], s[c + 5]);
-          a3 = fmax3(a3, s[c + 6], s[c + 7]);
-        }
-        const float m_blk = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * cj;
-        float alpha = 1.f;
-        bool moved = false;
-        if (m_blk > m_use + kRescaleThreshold) {
-          alpha = ex2_approx(m_use - m_blk);  // 0 when m_use = -inf
-          m_use = m_blk;
-          moved = true;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, moved)) {
-          // O_t row *= alpha (alpha = 1 for rows whose max did not move).  The
-          // previous P_t V product has completed: s_full was committed after it.
+          for (int b = 0; b < 4; ++b) {
+            float g4[4];
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32_wait(tO + c0, o);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st32(tO + c0, o);
+            for (int q = 0; q < 4; ++q) {
+              const float* x = s + 32 * b + 8 * q;
+              g4[q] = fmaxf(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], fmax3(x[5], x[6], x[7])));
+            }
+            bm[b] = fmaxf(fmaxf(g4[0], g4[1]), fmaxf(g4[2], g4[3]));
           }
-        }
-        // P = 2^(s * cj - m [+ off]), summed in four independent pairs of lanes
-        const float m_sub = ((m_use == -INFINITY) ? 0.f : m_use) - off;
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
-        uint32_t pk[kBlockN / 2];
+          // E_b = ceil(max t) (base 2; -inf for a block without a visible key)
+          float eb[4];
 #pragma unroll
-        for (int c = 0; c < kBlockN; c += 2) {
-          const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(cj, cj), make_float2(-m_sub, -m_sub));
-          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
-          if constexpr (kFp8) pk[c / 2] = pack_f16x2(e.x, e.y);
-          else pk[c / 2] = pack_bf16x2(e.x, e.y);
+          for (int b = 0; b < 4; ++b) eb[b] = ceilf(bm[b] * cj);
+          // codes e2m1(2^(t - E_b + 2)), eight per 32-bit column (key k in bits
+          // 4 (k % 8)), and each block's sum of code values (exact f16 sums of at
+          // most 96).  They depend on the scores alone, so they are formed before
+          // the running max moves, and the scores die here.
+          uint32_t w[16];
+          float bsum[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const float add = eb[b] > -INFINITY ? 2.f - eb[b] : 0.f;
+            uint32_t hs = 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t word = 0u;
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                const int c = 32 * b + 8 * q + e;
+                const float2 y = ffma2(make_float2(s[c], s[c + 1]), make_float2(cj, cj), make_float2(add, add));
+                const uint32_t byte = cvt_e2m1x2(ex2_approx(y.x), ex2_approx(y.y));
+                word |= byte << (4 * e);
+                hs = hadd2_u32(hs, e2m1x2_to_f16x2(byte));
+              }
+              w[4 * b + q] = word;
+            }
+            bsum[b] = f16x2_sum(hs);
+          }
+          const float e_max = fmaxf(fmaxf(eb[0], eb[1]), fmaxf(eb[2], eb[3]));
+          float alpha = 1.f;
+          bool moved = false;
+          if (e_max > m_use + kRescaleThreshold) {
+            alpha = exp2_int(m_use - e_max);  // a whole power of two; 0 when m_use = -inf
+            m_use = e_max;
+            moved = true;
+          }
+          if (j > 0 && __any_sync(0xffffffffu, moved)) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32_wait(tO + c0, o);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              tmem_st32(tO + c0, o);
+            }
+          }
+          // block scales 2^(E_b - 2 - m) as E8M0 bytes, and the row sum
+          float rowsum = 0.f;
+          uint32_t sfa = 0u;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const bool empty = !(eb[b] > -INFINITY);
+            const float rel = empty ? -INFINITY : eb[b] - 2.f - m_use;
+            rowsum += bsum[b] * exp2_int(rel);
+            const int sbyte = empty ? 0 : max(0, min(254, static_cast<int>(rel) + 127));
+            sfa |= static_cast<uint32_t>(sbyte) << (8 * b);
+          }
+          l = l * alpha + rowsum;
+          // P at S_t columns 0..15; columns 32..35: this row's P scales (every
+          // column the MMA may read for it); 64..67: the V^T scale words of
+          // channels lane + 32 c
+          uint32_t sa4[4], sb4[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            sa4[c] = sfa;
+            sb4[c] = __ldg(reinterpret_cast<const uint32_t*>(p.v_scale) + vts_idx + 32u * c * vts_stride + jb);
+          }
+          tmem_st16(tS, w);
+          tmem_st4(tS + kFp4SfaCol, sa4);
+          tmem_st4(tS + kFp4SfbCol, sb4);
+        } else {
+          // row max: four independent chains of three-input max
+          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+  #pragma unroll
+          for (int c = 4; c < kBlockN; c += 8) {
+            a0 = fmax3(a0, s[c], s[c + 1]);
+            a1 = fmax3(a1, s[c + 2], s[c + 3]);
+            a2 = fmax3(a2, s[c + 4], s[c + 5]);
+            a3 = fmax3(a3, s[c + 6], s[c + 7]);
+          }
+          const float m_blk = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * cj;
+          float alpha = 1.f;
+          bool moved = false;
+          if (m_blk > m_use + kRescaleThreshold) {
+            alpha = ex2_approx(m_use - m_blk);  // 0 when m_use = -inf
+            m_use = m_blk;
+            moved = true;
+          }
+          if (j > 0 && __any_sync(0xffffffffu, moved)) {
+            // O_t row *= alpha (alpha = 1 for rows whose max did not move).  The
+            // previous P_t V product has completed: s_full was committed after it.
+  #pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32_wait(tO + c0, o);
+  #pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              tmem_st32(tO + c0, o);
+            }
+          }
+          // P = 2^(s * cj - m [+ off]), summed in four independent pairs of lanes
+          const float m_sub = ((m_use == -INFINITY) ? 0.f : m_use) - off;
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+          uint32_t pk[kBlockN / 2];
+  #pragma unroll
+          for (int c = 0; c < kBlockN; c += 2) {
+            const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(cj, cj), make_float2(-m_sub, -m_sub));
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
+            if constexpr (kFp8) pk[c / 2] = pack_f16x2(e.x, e.y);
+            else pk[c / 2] = pack_bf16x2(e.x, e.y);
+          }
+          const float2 acc01 = fadd2(acc[0], acc[1]);
+          const float2 acc23 = fadd2(acc[2], acc[3]);
+          const float2 accs = fadd2(acc01, acc23);
+          float rowsum = accs.x + accs.y;
+          if constexpr (kFp8) rowsum *= ex2_approx(-off);  // back to the unscaled P
+          l = l * alpha + rowsum;
+          tmem_st64(tS, pk);
         }
-        const float2 acc01 = fadd2(acc[0], acc[1]);
-        const float2 acc23 = fadd2(acc[2], acc[3]);
-        const float2 accs = fadd2(acc01, acc23);
-        float rowsum = accs.x + accs.y;
-        if constexpr (kFp8) rowsum *= ex2_approx(-off);  // back to the unscaled P
-        l = l * alpha + rowsum;
-        tmem_st64(tS, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_p_full + 8 * t);
@@ -640,7 +777,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         if (!(ok = warp_wait(b_pv_done + 8 * t, pv_iter & 1, abort_flag, tmo, p.err, 22 + t))) break;
         ++pv_iter;
         tc_fence_after();
-        const float inv_l = (kFp8 ? sv_max * (1.f / 64.f) : 1.f) / l;
+        const float inv_l = ((kFp8 && !kFp4) ? sv_max * (1.f / 64.f) : 1.f) / l;
         const size_t r = static_cast<size_t>(bh) * p.Nq + row;
         uint4* dst = reinterpret_cast<uint4*>(p.o + r * D);
         // O in 64-column halves (fewer live registers); the last load frees O_t

@@ -167,6 +167,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor for a K-major operand in the 64-byte swizzled layout (the
+// TMA SWIZZLE_64B image of a tile with 64-byte rows): eight rows form a 512-byte
+// atom; layout code 4.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 4ull << 61;
+  return d;
+}
+
 // Instruction descriptor (32 bit) of a dense tcgen05.mma:
 //   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format
 //   [15] A major (0 = K-major)  [16] B major (1 = MN-major)
@@ -217,6 +230,33 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Block-scaled FP4 (MXFP4: e2m1 elements, one E8M0 scale per 32 K elements),
+// kind::mxf4, scale_vec::2X, K = 64 per instruction, both operands K-major.
+// Instruction descriptor: [4,6) B scale-factor id, [7,10) A format (e2m1 = 1),
+// [10,13) B format, [17,23) N >> 3, [23] scale format (1 = E8M0), [24,29)
+// M >> 4, [29,31) A scale-factor id.  The id selects the byte of the 32-bit
+// scale words where this instruction's two scales start: 0 for K elements
+// 0..63 of a 128-element row, 2 for 64..127 (1 and 3 are not valid for 2X).
+// Scale words in TMEM: for row r of A (and of B), the word holding its four
+// 32-element block scales sits in column base + r / 32 of lane r % 32 of the
+// lane quadrant the MMA reads, for A the row's own lane, for B every quadrant.
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(uint32_t M, uint32_t N, uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+         (sf_id << 29);
+}
+
+// D[tmem] (+)= (A[tmem] * sA) (B[smem] * sB)^T with A = 8 e2m1 per 32-bit column
+// (element k of a row in bits 4 (k % 8) of column k / 8).
+__device__ __forceinline__ void mma_mxf4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], [%1], %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 
@@ -309,6 +349,37 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
       : "=r"(r)
       : "f"(a), "f"(b), "f"(c), "f"(d));
   return r;
+}
+
+// Two floats -> two e2m1 codes in one byte (round to nearest even, saturating to
+// +-6); `lo` lands in bits 0..3.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// One byte of two e2m1 codes -> f16x2 (exact); bits 0..3 -> the low half.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Sum of the two halves of an f16x2 word, in fp32.
+__device__ __forceinline__ float f16x2_sum(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(h));
+  return lo + hi;
+}
+// 2^n for an integer-valued float n (exact; 0 below 2^-126).
+__device__ __forceinline__ float exp2_int(float n) {
+  return n < -126.f ? 0.f : __int_as_float((static_cast<int>(n) + 127) << 23);
 }
 
 }  // namespace attn

@@ -171,6 +171,27 @@ int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o
 size_t attn_splitkv_static_scratch_bytes(void);
 
 /*
+ * attn_fwd_fp4p -- Direct-P FP4 forward (the "Hardware-Aware FP4
+ * FlashAttention-4" summary: Direct-P for non-causal inference on Blackwell's
+ * FP4 tensor cores).  Q K^T as in attn_fwd_fp8; P V on the FP4 tensor cores with
+ * V in MXFP4 and P mapped from the scores straight to e2m1 codes: for every row
+ * and every block of 32 keys, E = ceil(max of the block's base-2 scores
+ * t = scale log2(e) s_q s_k q.k), code = e2m1 round-to-nearest-even of
+ * 2^(t - E + 2), p = value(code) 2^(E - 2); O = sum p v / sum p and
+ * lse = ln(sum p).  An approximation of attention (4-bit probabilities).
+ *   q8, k8     : e4m3 [B,H,N,d]; q_scale, k_scale fp32 [B,H,N/128] as attn_fwd_fp8
+ *   vt4        : V^T as MXFP4 codes, uint8 [B,H,d,N/2] (key 2i in the low nibble
+ *                of byte i), 16-byte aligned
+ *   vt_scale   : E8M0 block scales of vt4, uint8 [B,H,d,N/32] (value 2^(byte-127)
+ *                for keys 32k..32k+31 of channel c), 4-byte aligned
+ *   o, lse     : bf16 [B,H,N,d] and fp32 [B,H,N] (lse may be NULL)
+ *   d = 128; N a multiple of 128 (else ATTN_ERR_DIMS); causal allowed.
+ */
+int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* q_scale, const float* k_scale,
+                  const unsigned char* vt_scale, void* o, float* lse, int B, int H, int N, int d, int causal,
+                  float scale, void* stream);
+
+/*
  * attn_bwd -- gradients of the BF16 attention forward (the training use the
  * FlashAttention-2 article reports under "Performance"):
  *   dV = P^T dO,  dS = P o (dP - D) with dP = dO V^T and D_i = do_i . o_i,

@@ -93,6 +93,20 @@ def test_fp8_validation_codes(lib):
     assert _call_fp8(lib, scale=0.0) == -10
 
 
+def test_fp4p_validation_codes(lib):
+    import exact_tiled_attention_16_gb300._lib as L
+
+    def call(d=128, N=256, vts=0x7000, qs=0x6000, q=0x1000, scale=0.1):
+        return L.attn_fwd_fp4p_raw(q, 0x2000, 0x3000, qs, 0x6100, vts, 0x4000, 0x5000, 1, 2, N, d, 0, scale, 0)
+    assert call(d=64) == -3
+    assert call(N=200) == -2   # N must be a multiple of 128
+    assert call(vts=0) == -1
+    assert call(vts=0x7002) == -5
+    assert call(qs=0) == -1
+    assert call(q=0) == -1
+    assert call(scale=0.0) == -10
+
+
 def test_partial_merge_splitkv_validation(lib):
     import exact_tiled_attention_16_gb300._lib as L
     P = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000)
