@@ -59,6 +59,7 @@ WORKLOAD_TEXT = {
     "cfg3": "bf16 B1 H32 N16384 d128 causal (long sequence, small batch)",
     "cfg4": "bf16 B16 H16 N4096 d64 non-causal, 2 shared Q/K outlier channels x20",
     "cfg5": "e4m3 block-scaled B2 H16 N8192 d128 non-causal, rotated Q/K",
+    "cfg5p": "Direct-P FP4: cfg5's Q/K (e4m3) with V in MXFP4 (e2m1, E8M0 per 32 keys), B2 H16 N8192 d128",
     "decode": "bf16 B2 H16 Nq512 Nk65536 d128 non-causal, split-K/V forward + merge",
 }
 DECODE = dict(B=2, H=16, Nq=512, Nk=65536, d=128, seed=6)
@@ -188,6 +189,8 @@ def cpu_oracle_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 256
     seconds of oracle time have passed; returns (TFLOP/s in the workload's
     counting convention, sample description, seconds)."""
     from oracle.attention import attention_head
+    from oracle.direct_p import direct_p_head
+    head_fn = direct_p_head if w.dtype == "e4m3_e2m1" else attention_head
     flops = 0.0
     elapsed = 0.0
     heads = 0
@@ -197,7 +200,7 @@ def cpu_oracle_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 256
             q, k, v = w.head_f64(b, h)
             rows = synth.sample_rows(q.shape[0], rows_per_head, w.seed, b, h)
             t0 = time.perf_counter()
-            attention_head(q, k, v, w.causal, w.scale, rows=rows)
+            head_fn(q, k, v, w.causal, w.scale, rows=rows)
             elapsed += time.perf_counter() - t0
             vis = (rows + 1) if w.causal else np.full(len(rows), w.N)
             flops += float(4.0 * w.d * vis.sum())
@@ -207,7 +210,8 @@ def cpu_oracle_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 256
                 break
         if elapsed >= budget_s or (max_heads and heads >= max_heads):
             break
-    desc = (f"{rows_done} query rows ({rows_per_head} seeded rows per head x {heads} heads) against all "
+    what = "Direct-P oracle: " if w.dtype == "e4m3_e2m1" else ""
+    desc = (f"{what}{rows_done} query rows ({rows_per_head} seeded rows per head x {heads} heads) against all "
             f"visible keys of {w.name}; fp64 numpy, {_CORES} BLAS threads")
     return flops / elapsed / 1e12, desc, elapsed
 
@@ -255,6 +259,7 @@ def run_reference(args, world, rank):
         w = synth.make_config(args.workload)
     from oracle.attention import attention_head
     from oracle.attention_bwd import attention_bwd_query_rows
+    from oracle.direct_p import direct_p_head
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     rows_per_step = 32
     bwd = args.bwd_pass == "bwd"
@@ -268,6 +273,8 @@ def run_reference(args, world, rank):
         t0 = time.perf_counter()
         if bwd:
             attention_bwd_query_rows(q, k, v, do, w.causal, w.scale, rows)
+        elif w.dtype == "e4m3_e2m1":
+            direct_p_head(q, k, v, w.causal, w.scale, rows=rows)
         else:
             attention_head(q, k, v, w.causal, w.scale, rows=rows)
         dt = time.perf_counter() - t0
@@ -354,7 +361,8 @@ def main():
         w = make_decode_workload()
     else:
         w = synth.make_config(args.workload)
-    fp8 = w.dtype == "e4m3"
+    fp4 = w.dtype == "e4m3_e2m1"
+    fp8 = w.dtype == "e4m3" or fp4
     bwd = args.bwd_pass == "bwd"
     if bwd and (fp8 or decode):
         raise SystemExit("--pass bwd runs on the bf16 square workloads (not the e4m3 one or decode)")
@@ -385,7 +393,9 @@ def main():
                          device=dev)
 
     def forward(qq, kk, vv, ss, oo=None, dd=None, ll=None):
-        if bwd:
+        if fp4:
+            pkg.attn_fwd_fp4p(qq, kk, vv, *ss, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        elif bwd:
             pkg.attn_bwd(qq, kk, vv, o if oo is None else oo, dout if dd is None else dd, lse if ll is None else ll,
                          causal=w.causal, scale=w.scale, dq=grads[0], dk=grads[1], dv=grads[2], workspace=bws)
         elif decode:
@@ -494,17 +504,27 @@ def main():
 
     peaks, peak_src = measured_peaks()
     # FP8 peak = measured bf16 x 2 (the nominal dense fp8/bf16 ratio, 4.5 / 2.25 PFLOP/s)
-    ratio = 2.0 if fp8 else 1.0
+    ratio = 2.0 if fp8 and not fp4 else 1.0
     peak = float(peaks["bf16_tflops"]) * ratio
     src = (f"{peak_src} bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json)" if peak_src == "measured"
            else "fallback 1.9 PFLOP/s bf16") + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else "")
-    kname = "attn_bwd: prep + dq + dkdv kernels (whole step)" if bwd else {("bf16", 64): "attn_fwd_kernel<64,4,4,false>", ("bf16", 128): "attn_fwd_kernel<128,2,2,false>",
+    kname = "attn_bwd: prep + dq + dkdv kernels (whole step)" if bwd else {("e4m3_e2m1", 128): "attn_fwd_kernel<128,4,4,fp8,final,fp4>",
+                                                                         ("bf16", 64): "attn_fwd_kernel<64,4,4,false>", ("bf16", 128): "attn_fwd_kernel<128,2,2,false>",
              ("e4m3", 128): "attn_fwd_kernel<128,3,3,true>"}.get((w.dtype, w.d), "attn_fwd_kernel")
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic_for(w.name + (":bwd" if bwd else "")), "peak_source": src,
             "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * ratio),
             "kernel": kname, "avg_launch_ms": avg_kernel_ms, "flops_per_launch": flops}
-    if fp8:
+    if fp4:
+        # Q K^T on the fp8 path (2x bf16), P V on the FP4 path (6x bf16: nominal
+        # 13.5 / 2.25 PFLOP/s): the roof of that mix is 1 / (0.5/fp8 + 0.5/fp4)
+        b16 = float(peaks["bf16_tflops"])
+        mixed = 1.0 / (0.5 / (2.0 * b16) + 0.5 / (6.0 * b16))
+        roof["peak"] = mixed
+        roof["frac"] = achieved / mixed
+        roof["peak_source"] = src + " x 3 (mixed roof: Q K^T at the nominal fp8 ratio 2, P V at the fp4 ratio 6)"
+        roof["frac_of_sustained"] = achieved / (float(peaks.get("bf16_tflops_sustained", b16)) * 3.0)
+    elif fp8:
         # Q K^T runs on the fp8 tensor path and P V on the 16-bit one: the roof of
         # that mix is flops / (flops/2 / fp8_peak + flops/2 / bf16_peak).
         mixed = 1.0 / (0.5 / peak + 0.5 / float(peaks["bf16_tflops"]))
@@ -516,7 +536,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) inputs)",
         "config": config_block(args, w),
-        "pct_of_peak": 100.0 * value / world / peak,
+        "pct_of_peak": 100.0 * value / world / roof["peak"],
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": int(sum(t.nbytes for t in in_host)),

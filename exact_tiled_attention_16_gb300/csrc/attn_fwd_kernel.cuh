@@ -650,29 +650,29 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
           for (int b = 0; b < 4; ++b) eb[b] = ceilf(bm[b] * cj);
           // codes e2m1(2^(t - E_b + 2)), eight per 32-bit column (key k in bits
-          // 4 (k % 8)), and each block's sum of code values (exact f16 sums of at
-          // most 96).  They depend on the scores alone, so they are formed before
+          // 4 (k % 8)), and each block's sum of code values (exact integers, in
+          // halves).  They depend on the scores alone, so they are formed before
           // the running max moves, and the scores die here.
           uint32_t w[16];
           float bsum[4];
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
             const float add = eb[b] > -INFINITY ? 2.f - eb[b] : 0.f;
-            uint32_t hs = 0u;
+            uint32_t sum2 = 0u;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              uint32_t word = 0u;
+              uint32_t by[4];
 #pragma unroll
               for (int e = 0; e < 8; e += 2) {
                 const int c = 32 * b + 8 * q + e;
                 const float2 y = ffma2(make_float2(s[c], s[c + 1]), make_float2(cj, cj), make_float2(add, add));
-                const uint32_t byte = cvt_e2m1x2(ex2_approx(y.x), ex2_approx(y.y));
-                word |= byte << (4 * e);
-                hs = hadd2_u32(hs, e2m1x2_to_f16x2(byte));
+                by[e / 2] = cvt_e2m1x2(ex2_approx(y.x), ex2_approx(y.y));
               }
+              const uint32_t word = pack_bytes4(by[0], by[1], by[2], by[3]);
               w[4 * b + q] = word;
+              sum2 = e2m1x8_sum2(word, sum2);
             }
-            bsum[b] = f16x2_sum(hs);
+            bsum[b] = 0.5f * static_cast<float>(sum2);
           }
           const float e_max = fmaxf(fmaxf(eb[0], eb[1]), fmaxf(eb[2], eb[3]));
           float alpha = 1.f;

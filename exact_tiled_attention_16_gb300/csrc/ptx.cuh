@@ -359,23 +359,19 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
       : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// One byte of two e2m1 codes -> f16x2 (exact); bits 0..3 -> the low half.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
-  return r;
+// Twice the sum of the eight e2m1 values held by a word of non-negative codes
+// (nibble k = code of element k), added to acc: a byte-permute table lookup of
+// 2 * value (0, 1, 2, 3, 4, 6, 8, 12 for codes 0..7), four bytes at a time, and
+// a four-way byte dot product.  Exact integers.
+__device__ __forceinline__ uint32_t e2m1x8_sum2(uint32_t word, uint32_t acc) {
+  const uint32_t lo = __byte_perm(0x03020100u, 0x0C080604u, word);
+  const uint32_t hi = __byte_perm(0x03020100u, 0x0C080604u, word >> 16);
+  acc = __dp4a(lo, 0x01010101u, acc);
+  return __dp4a(hi, 0x01010101u, acc);
 }
-__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-// Sum of the two halves of an f16x2 word, in fp32.
-__device__ __forceinline__ float f16x2_sum(uint32_t h) {
-  float lo, hi;
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi) : "r"(h));
-  return lo + hi;
+// Four code bytes (each in the low byte of a word) -> one word, b0 lowest.
+__device__ __forceinline__ uint32_t pack_bytes4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
 }
 // 2^n for an integer-valued float n (exact; 0 below 2^-126).
 __device__ __forceinline__ float exp2_int(float n) {

@@ -381,6 +381,9 @@ CONFIGS = {
                  qk_outlier_frac=0.02, qk_outlier_mult=20.0),
     "cfg5": dict(kind="e4m3", B=2, H=16, N=8192, d=128, causal=False, seed=5,
                  outlier_frac=0.01, outlier_mult=10.0),
+    # the Direct-P FP4 path on cfg5's shape and draw: Q, K e4m3, V MXFP4
+    "cfg5p": dict(kind="e4m3_e2m1", B=2, H=16, N=8192, d=128, causal=False, seed=5,
+                  outlier_frac=0.01, outlier_mult=10.0),
 }
 
 
@@ -389,6 +392,8 @@ def make_config(name: str) -> Workload:
     kind = c.pop("kind")
     if kind == "bf16":
         return make_bf16(name=name, **c)
+    if kind == "e4m3_e2m1":
+        return make_fp4p(name=name, **c)
     return make_fp8(name=name, **c)
 
 
