@@ -40,6 +40,10 @@ def load_library():
     lib.attn_fwd.restype = ci
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
     lib.attn_fwd_fp8.restype = ci
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, ctypes.c_size_t, vp]
+    lib.attn_fwd_host.restype = ci
+    lib.attn_fwd_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_fwd_fp4p.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
     lib.attn_fwd_fp4p.restype = ci
     lib.attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, vp]
@@ -149,6 +153,49 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sc
                           B, H, N, d, causal, scale, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8")
+    return o, lse
+
+
+def fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().attn_fwd_host_workspace_bytes(B, H, N, d))
+
+
+def attn_fwd_host_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int, causal: bool,
+                      scale: float, workspace: int, workspace_bytes: int, stream: int) -> int:
+    return load_library().attn_fwd_host(q or None, k or None, v or None, o or None, lse or None, B, H, N, d,
+                                        1 if causal else 0, float(scale), workspace or None, int(workspace_bytes),
+                                        stream or None)
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+                  want_lse: bool = True, workspace=None, stream=None):
+    """attn_fwd on HOST tensors q, k, v [B,H,N,d] bf16 (page-locked for full
+    speed); transfers and kernels are pipelined by the library.  Returns host
+    (o, lse), valid once `stream` (default: torch's current stream) has
+    completed.  The device workspace is allocated with torch when not given."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous host bf16 tensor [B,H,N,d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape [B,H,N,d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q.is_pinned()
+    if o is None:
+        o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    need = fwd_host_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = attn_fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr() if lse is not None else 0, B, H, N, d, causal, scale,
+                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                           _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
     return o, lse
 
 

@@ -148,6 +148,55 @@ int make_map_vt4(CUtensorMap* map, const void* ptr, int d, int N, int BH) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_OVERFLOW;
 }
 
+// Pipelined forward over host buffers: the heads go in chunks through two slots of
+// a device workspace; copy-in, kernel and copy-out run on three streams, so the
+// transfers of one chunk overlap the kernel of another.
+constexpr int kHostChunks = 8;  // measured: 8 beats 3, 4, 6, 12, 16 on the large workloads
+constexpr int kHostSlots = 2;
+
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t entry = nullptr, last = nullptr;
+  cudaEvent_t in_done[kHostSlots] = {}, comp_done[kHostSlots] = {}, out_done[kHostSlots] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+int pipe_setup(HostPipe& hp) {
+  if (hp.ready) return ATTN_OK;
+  const unsigned kEv = cudaEventDisableTiming;
+  if (cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&hp.entry, kEv) != cudaSuccess ||
+      cudaEventCreateWithFlags(&hp.last, kEv) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  for (int i = 0; i < kHostSlots; ++i)
+    if (cudaEventCreateWithFlags(&hp.in_done[i], kEv) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.comp_done[i], kEv) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.out_done[i], kEv) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  hp.ready = true;
+  return ATTN_OK;
+}
+
+struct HostChunking {
+  int heads;          // heads per chunk (the last chunk may hold fewer)
+  int chunks;
+  size_t slot_bytes;  // Q, K, V and O of a chunk (bf16) and its LSE (fp32), 256-byte aligned
+};
+HostChunking host_chunking(int B, int H, int N, int d) {
+  HostChunking hc;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n = BH < kHostChunks ? BH : kHostChunks;
+  hc.heads = static_cast<int>((BH + n - 1) / n);
+  hc.chunks = static_cast<int>((BH + hc.heads - 1) / hc.heads);
+  const size_t t = static_cast<size_t>(hc.heads) * N * d * 2;  // one bf16 tensor of a chunk (multiple of 128)
+  const size_t l = (static_cast<size_t>(hc.heads) * N * sizeof(float) + 255) / 256 * 256;
+  hc.slot_bytes = 4 * t + l;
+  return hc;
+}
+
 // Largest sequence length accepted: keeps every position and mask limit of the
 // kernels inside 32-bit integers.
 constexpr long long kMaxSeq = 1ll << 30;
@@ -290,6 +339,72 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   return launch_bf16(q, k, v, d, false, p, dev, stream);
+}
+
+size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  return kHostSlots * host_chunking(B, H, N, d).slot_bytes;
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_tensors(q, k, v, o, lse, B, H, N, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (!workspace) return ATTN_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
+  const HostChunking hcfg = host_chunking(B, H, N, d);
+  if (workspace_bytes < kHostSlots * hcfg.slot_bytes) return ATTN_ERR_DIMS;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  HostPipe& hp = g_pipe[dev];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  if ((rc = pipe_setup(hp)) != ATTN_OK) return rc;
+  cudaStream_t sc = static_cast<cudaStream_t>(stream);
+  const long long BH = static_cast<long long>(B) * H;
+  const size_t head_bytes = static_cast<size_t>(N) * d * 2;
+  const size_t chunk_in = static_cast<size_t>(hcfg.heads) * head_bytes;
+  bool ok = true;
+  auto ck = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+  // the copies wait for earlier work on the caller's stream (it may still use the workspace)
+  ck(cudaEventRecord(hp.entry, sc));
+  ck(cudaStreamWaitEvent(hp.s_in, hp.entry, 0));
+  ck(cudaStreamWaitEvent(hp.s_out, hp.entry, 0));
+  for (int c = 0; c < hcfg.chunks && ok; ++c) {
+    const int slot = c % kHostSlots;
+    const long long h0 = static_cast<long long>(c) * hcfg.heads;
+    const int hn = static_cast<int>(BH - h0 < hcfg.heads ? BH - h0 : hcfg.heads);
+    const size_t bytes = static_cast<size_t>(hn) * head_bytes;
+    uint8_t* base = static_cast<uint8_t*>(workspace) + slot * hcfg.slot_bytes;
+    uint8_t *dq = base, *dk = dq + chunk_in, *dv = dk + chunk_in, *dout = dv + chunk_in;
+    float* dl = reinterpret_cast<float*>(dout + chunk_in);
+    // copy in, once the kernel two chunks back is done with this slot's inputs
+    if (c >= kHostSlots) ck(cudaStreamWaitEvent(hp.s_in, hp.comp_done[slot], 0));
+    ck(cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + h0 * head_bytes, bytes, cudaMemcpyHostToDevice, hp.s_in));
+    ck(cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + h0 * head_bytes, bytes, cudaMemcpyHostToDevice, hp.s_in));
+    ck(cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + h0 * head_bytes, bytes, cudaMemcpyHostToDevice, hp.s_in));
+    ck(cudaEventRecord(hp.in_done[slot], hp.s_in));
+    // the kernel, once the inputs are in and the copy-out two chunks back has read the outputs
+    ck(cudaStreamWaitEvent(sc, hp.in_done[slot], 0));
+    if (c >= kHostSlots) ck(cudaStreamWaitEvent(sc, hp.out_done[slot], 0));
+    if (!ok) break;
+    FwdParams p;
+    fill_params(p, hn, N, N, causal, 0, 0, 1, scale, dev);
+    p.o = reinterpret_cast<__nv_bfloat16*>(dout);
+    p.lse = lse ? dl : nullptr;
+    if ((rc = launch_bf16(dq, dk, dv, d, false, p, dev, sc)) != ATTN_OK) return rc;
+    ck(cudaEventRecord(hp.comp_done[slot], sc));
+    // copy out
+    ck(cudaStreamWaitEvent(hp.s_out, hp.comp_done[slot], 0));
+    ck(cudaMemcpyAsync(static_cast<uint8_t*>(o) + h0 * head_bytes, dout, bytes, cudaMemcpyDeviceToHost, hp.s_out));
+    if (lse)
+      ck(cudaMemcpyAsync(lse + h0 * N, dl, static_cast<size_t>(hn) * N * sizeof(float), cudaMemcpyDeviceToHost,
+                         hp.s_out));
+    ck(cudaEventRecord(hp.out_done[slot], hp.s_out));
+  }
+  // work queued on the caller's stream after this call sees the outputs in host memory
+  ck(cudaEventRecord(hp.last, hp.s_out));
+  ck(cudaStreamWaitEvent(sc, hp.last, 0));
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,

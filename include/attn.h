@@ -171,6 +171,25 @@ int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o
 size_t attn_splitkv_static_scratch_bytes(void);
 
 /*
+ * attn_fwd_host -- attn_fwd with Q, K, V, O and LSE in HOST memory (page-locked
+ * for full speed).  The B*H heads go through the device in up to eight chunks of
+ * whole heads; the host->device copies of one chunk, the kernel of another and
+ * the device->host copies of a third run on separate streams, so the transfers
+ * overlap the computation.  Outputs are bitwise those of attn_fwd.
+ *   workspace : device scratch of at least attn_fwd_host_workspace_bytes(B,H,N,d)
+ *               bytes, 256-byte aligned, owned by the caller; the call overwrites it
+ *   stream    : the kernels run on it; work queued on it after this call sees
+ *               the outputs in host memory.  Calls that share a workspace must
+ *               be queued on the same stream.
+ * Other arguments and errors as attn_fwd (BF16 only).
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device scratch attn_fwd_host needs (0 for invalid arguments). */
+size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * attn_fwd_fp4p -- Direct-P FP4 forward (the "Hardware-Aware FP4
  * FlashAttention-4" summary: Direct-P for non-causal inference on Blackwell's
  * FP4 tensor cores).  Q K^T as in attn_fwd_fp8; P V on the FP4 tensor cores with

@@ -107,6 +107,24 @@ def test_fp4p_validation_codes(lib):
     assert call(scale=0.0) == -10
 
 
+def test_fwd_host_validation(lib):
+    import exact_tiled_attention_16_gb300._lib as L
+    need = L.fwd_host_workspace_bytes(2, 3, 100, 64)
+    # six heads, one per chunk (at most eight chunks): two slots of Q, K, V, O (100 x 64
+    # bf16 each) and the chunk's LSE (400 bytes) rounded up to 256 bytes
+    assert need == 2 * (4 * 100 * 64 * 2 + 512)
+    # 32 heads in eight chunks of four
+    assert L.fwd_host_workspace_bytes(1, 32, 256, 128) == 2 * (4 * 4 * 256 * 128 * 2 + 4096)
+    assert L.fwd_host_workspace_bytes(1, 1, 100, 96) == 0
+
+    def call(ws=0x10000, nbytes=need, d=64):
+        return L.attn_fwd_host_raw(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 2, 3, 100, d, 0, 0.125, ws, nbytes, 0)
+    assert call(ws=0) == -1
+    assert call(ws=0x10010) == -5
+    assert call(nbytes=need - 1) == -2
+    assert call(d=96) == -3
+
+
 def test_partial_merge_splitkv_validation(lib):
     import exact_tiled_attention_16_gb300._lib as L
     P = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000)

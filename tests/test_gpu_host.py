@@ -1,0 +1,79 @@
+"""attn_fwd_host: the forward on host buffers, with transfers and kernels
+pipelined in chunks of heads, gives bitwise the outputs of attn_fwd on the same
+inputs (each chunk runs the same kernel on whole heads), with pinned or pageable
+host memory, ragged last chunks, without LSE, and on back-to-back calls that
+share the workspace."""
+import numpy as np
+import pytest
+
+from exact_tiled_attention_16_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_tiled_attention_16_gb300 as pkg
+    pkg.load_library()
+
+
+def _host(bits, pin):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory() if pin else t.clone()
+
+
+SHAPES = [(1, 1, 200, 64, False), (2, 3, 333, 128, True), (1, 5, 1000, 64, True), (2, 16, 512, 128, False),
+          (1, 7, 129, 128, True)]
+
+
+@pytest.mark.parametrize("pin", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{b}H{h}N{n}d{d}{'c' if c else 'n'}" for b, h, n, d, c in SHAPES])
+def test_bitwise_equal_to_device_call(shape, pin):
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d, causal = shape
+    w = synth.make_bf16(B, H, N, d, causal, seed=600 + N)
+    qh, kh, vh = (_host(x, pin) for x in (w.q, w.k, w.v))
+    o_h, l_h = pkg.attn_fwd_host(qh, kh, vh, causal=causal, scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    o_d, l_d = pkg.attn_fwd(qh.cuda(), kh.cuda(), vh.cuda(), causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h.view(torch.int16), o_d.cpu().view(torch.int16))
+    assert torch.equal(l_h.view(torch.int32), l_d.cpu().view(torch.int32))
+    assert pkg.check_device_errors()[0] == 0
+
+
+def test_without_lse_and_back_to_back_calls():
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d = 2, 6, 700, 128
+    ws = torch.empty(pkg.fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    outs = []
+    ins = []
+    for seed in (1, 2, 3):
+        w = synth.make_bf16(B, H, N, d, seed == 2, seed=seed)
+        qh, kh, vh = (_host(x, True) for x in (w.q, w.k, w.v))
+        o, lse = pkg.attn_fwd_host(qh, kh, vh, causal=w.causal, scale=w.scale, want_lse=False, workspace=ws)
+        assert lse is None
+        outs.append(o)
+        ins.append((qh, kh, vh, w))
+    torch.cuda.current_stream().synchronize()
+    for o, (qh, kh, vh, w) in zip(outs, ins):
+        o_d, _ = pkg.attn_fwd(qh.cuda(), kh.cuda(), vh.cuda(), causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), o_d.cpu().view(torch.int16))
+
+
+def test_workspace_too_small_launches_nothing():
+    import exact_tiled_attention_16_gb300._lib as L
+    q = torch.zeros(1, 2, 256, 64, dtype=torch.bfloat16).pin_memory()
+    o = torch.full_like(q, 7.0)
+    need = L.fwd_host_workspace_bytes(1, 2, 256, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    rc = L.attn_fwd_host_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), 0, 1, 2, 256, 64, 0, 0.125,
+                             ws.data_ptr(), need - 256, torch.cuda.current_stream().cuda_stream)
+    assert rc == -2
+    torch.cuda.synchronize()
+    assert (o.float() == 7.0).all()
