@@ -113,24 +113,28 @@ struct BwdSmem {
 // acc (+)= A B with A = 128 x 128 bf16 in TMEM (two keys per column) laid out as
 // the compute warpgroups write it: keys 0..63 in columns a_region + 0..31,
 // keys 64..127 in a_region + 64..95; B = 128 rows x D at b_base, MN-major.
+// (Descriptors as 32-bit low words: step kk adds its byte offset >> 4 to the
+// address field, which never carries since shared memory stays below 2^18.)
 template <typename L>
 __device__ __forceinline__ void bwd_issue_ts(uint32_t acc, uint32_t a_region, uint32_t b_base, uint32_t idesc,
                                              bool accumulate) {
+  const uint32_t b0 = sdesc_lo(b_base, L::kChunkBytes);
+  constexpr uint32_t hi = sdesc_hi_sw128(1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_f16_ts(acc, a_region + (kk >> 2) * 64 + (kk & 3) * 8,
-               sdesc_sw128(b_base + kk * 16 * 128, L::kChunkBytes, 1024), idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+    mma_f16_ts_w(acc, a_region + (kk >> 2) * 64 + (kk & 3) * 8, b0 + ((kk * 16 * 128) >> 4), hi, idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // C = A B^T with A, B 128 x D K-major bf16 tiles.
 template <int D, typename L>
 __device__ __forceinline__ void bwd_issue_ss(uint32_t c_tmem, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
+  const uint32_t a0 = sdesc_lo(a_base, 16), b0 = sdesc_lo(b_base, 16);
+  constexpr uint32_t hi = sdesc_hi_sw128(1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-    mma_f16_ss(c_tmem, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), idesc,
-               kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+    mma_f16_ss_w(c_tmem, a0 + off, b0 + off, hi, idesc, kk > 0 ? 1u : 0u);
   }
 }
 

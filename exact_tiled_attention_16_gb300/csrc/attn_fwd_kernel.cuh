@@ -401,15 +401,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       // 128-byte swizzled row, then on to the next column chunk.
       auto issue_s = [&](int t, uint32_t sk) {
         const uint32_t d_tmem = tmem + kTmemS[t];
-        const uint32_t q_base = sQ + t * L::kTileBytes;
-        const uint32_t k_base = sK + sk * L::kTileBytes;
+        // descriptor low words of step 0; step kk adds its byte offset >> 4 (the
+        // address field is 14 bits of address >> 4 and shared memory stays below
+        // 2^18 bytes, so the sum never carries into the LBO field)
+        const uint32_t qa0 = sdesc_lo(sQ + t * L::kTileBytes, 16);
+        const uint32_t kb0 = sdesc_lo(sK + sk * L::kTileBytes, 16);
+        constexpr uint32_t hi = sdesc_hi_sw128(1024);
 #pragma unroll
         for (int kk = 0; kk < D / (int)L::kMmaK; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          const uint64_t da = sdesc_sw128(q_base + off, 16, 1024);
-          const uint64_t db = sdesc_sw128(k_base + off, 16, 1024);
-          if constexpr (kFp8) mma_f8_ss(d_tmem, da, db, idesc_s, kk > 0 ? 1u : 0u);
-          else mma_f16_ss(d_tmem, da, db, idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+          if constexpr (kFp8) mma_f8_ss_w(d_tmem, qa0 + off, kb0 + off, hi, idesc_s, kk > 0 ? 1u : 0u);
+          else mma_f16_ss_w(d_tmem, qa0 + off, kb0 + off, hi, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(b_s_full + 8 * t);
       };
@@ -426,11 +428,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         make_idesc_mxf4(kBlockM, D, 2 * kk), tmem + kTmemS[t] + kFp4SfaCol,
                         tmem + kTmemS[t] + kFp4SfbCol, (accumulate || kk > 0) ? 1u : 0u);
         } else {
+          const uint32_t vb0 = sdesc_lo(v_base, LV::kChunkBytes);
+          constexpr uint32_t hi = sdesc_hi_sw128(1024);
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_f16_ts(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8,
-                       sdesc_sw128(v_base + kk * 16 * 128, LV::kChunkBytes, 1024), idesc_o,
-                       (accumulate || kk > 0) ? 1u : 0u);
+            mma_f16_ts_w(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8, vb0 + ((kk * 16 * 128) >> 4), hi, idesc_o,
+                         (accumulate || kk > 0) ? 1u : 0u);
         }
       };
       int o_uses[2] = {0, 0};  // units in which tile t has written O_t
