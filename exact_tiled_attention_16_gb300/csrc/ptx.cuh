@@ -157,15 +157,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 // 8-row atoms, LBO the distance between consecutive 128-byte-wide column blocks
 // of an MN-major operand.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
 
 // The descriptor split in two 32-bit words: the low word carries the start
 // address and LBO (the only fields that change from one MMA step to the next),
@@ -177,9 +168,9 @@ __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes)
   return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
 
-// The same descriptor for a K-major operand in the 64-byte swizzled layout (the
-// TMA SWIZZLE_64B image of a tile with 64-byte rows): eight rows form a 512-byte
-// atom; layout code 4.
+// A whole 64-bit descriptor (the format above) for a K-major operand in the
+// 64-byte swizzled layout (the TMA SWIZZLE_64B image of a tile with 64-byte
+// rows): eight rows form a 512-byte atom; layout code 4.
 __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
@@ -200,31 +191,11 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t M, uint32_t N, uint32
          ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16.  A is M x K with row m in lane m and
-// two 16-bit K elements per 32-bit column.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two forms with descriptors given as 32-bit low words and a shared
-// constant high word.
+// tcgen05.mma with shared-memory operands given by descriptor low words and a
+// shared constant high word (joined to 64 bits inside the asm):
+//   _ss: D[tmem] (+)= A[smem] B[smem]^T;  _ts: D[tmem] (+)= A[tmem] B[smem], A as
+//   M x K with row m in lane m and two 16-bit K elements per 32-bit column.
+// kind::f16 (bf16 or f16 operands) or kind::f8f6f4 (e4m3), fp32 accumulate.
 __device__ __forceinline__ void mma_f16_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -253,26 +224,6 @@ __device__ __forceinline__ void mma_f8_ss_w(uint32_t d_tmem, uint32_t a_lo, uint
       "setp.ne.b32 p, %5, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
       "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Same two forms for 8-bit floating-point inputs (kind::f8f6f4, fp32 accumulate).
-__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -382,18 +333,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_to_f16x2(uint16_t codes) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Four floats -> packed e4m3x4 (round to nearest even, saturating); a in bits 0..7.
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
-      "mov.b32 %0, {lo, hi};\n\t}"
-      : "=r"(r)
-      : "f"(a), "f"(b), "f"(c), "f"(d));
-  return r;
-}
-
 // Two floats -> two e2m1 codes in one byte (round to nearest even, saturating to
 // +-6); `lo` lands in bits 0..3.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
