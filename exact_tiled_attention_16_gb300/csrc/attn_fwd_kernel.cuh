@@ -721,9 +721,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           tmem_st4(tS + kFp4SfbCol, sb4);
         } else {
           // row max: four independent chains of three-input max
-          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-  #pragma unroll
-          for (int c = 4; c < kBlockN; c += 8) {
+          float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]), a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
+#pragma unroll
+          for (int c = 8; c < kBlockN; c += 8) {
             a0 = fmax3(a0, s[c], s[c + 1]);
             a1 = fmax3(a1, s[c + 2], s[c + 3]);
             a2 = fmax3(a2, s[c + 4], s[c + 5]);
@@ -740,11 +740,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           if (j > 0 && __any_sync(0xffffffffu, moved)) {
             // O_t row *= alpha (alpha = 1 for rows whose max did not move).  The
             // previous P_t V product has completed: s_full was committed after it.
-  #pragma unroll
+#pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t o[32];
               tmem_ld32_wait(tO + c0, o);
-  #pragma unroll
+#pragma unroll
               for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
               tmem_st32(tO + c0, o);
             }
@@ -754,7 +754,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                            make_float2(0.f, 0.f)};
           uint32_t pk[kBlockN / 2];
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < kBlockN; c += 2) {
             const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(cj, cj), make_float2(-m_sub, -m_sub));
             const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
