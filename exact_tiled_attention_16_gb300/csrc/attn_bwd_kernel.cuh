@@ -188,6 +188,8 @@ __device__ __forceinline__ void bwd_producer_drain(bool ok, uint32_t ga, uint32_
 
 // Bounded wait + abort plumbing shared by the two passes
 #define ATTN_BWD_WAIT(bar, par, where) mbar_wait((bar), (par), abort_flag, tmo, p.err, (where))
+// the same, taken by a whole warp (same answer on every lane)
+#define ATTN_BWD_WAIT_W(bar, par, where) warp_wait((bar), (par), abort_flag, tmo, p.err, (where))
 
 // ---------------------------------------------------------------------------
 // dQ pass.  TMEM: S at 0, dP at 128 (each warpgroup's dS, bf16, over the first
@@ -302,7 +304,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       bwd_producer_drain<RA, RB>(ok, ga, gb, units, rg, b_qd_full, b_qd_empty, abort_flag, tmo, p.err, 43);
     }
   } else if (warp == kBwdMmaWarp) {
-    if (lane == 0) {
+    {  // whole warp, warp-uniform; one elected lane issues each MMA and commit
       constexpr uint32_t idesc_ss = make_idesc(kBlockM, kBlockN, 1, false);  // bf16, K-major A and B
       constexpr uint32_t idesc_dq = make_idesc(kBlockM, D, 1, true);        // B = K, MN-major
       uint32_t g = 0, s_iter = 0, ds_iter = 0;
@@ -313,15 +315,15 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         if (u < 0) break;
         int bh, qb, nkv;
         unit(u, bh, qb, nkv);
-        if (!(ok = ATTN_BWD_WAIT(b_qd_full, units & 1, 50))) break;
+        if (!(ok = ATTN_BWD_WAIT_W(b_qd_full, units & 1, 50))) break;
         {  // S_0 and dP_0
-          if (!(ok = ATTN_BWD_WAIT(rg.a_full + 8 * (g % RA), (g / RA) & 1, 51))) break;
-          if (s_iter > 0 && !(ok = ATTN_BWD_WAIT(b_s_free, (s_iter - 1) & 1, 52))) break;
+          if (!(ok = ATTN_BWD_WAIT_W(rg.a_full + 8 * (g % RA), (g / RA) & 1, 51))) break;
+          if (s_iter > 0 && !(ok = ATTN_BWD_WAIT_W(b_s_free, (s_iter - 1) & 1, 52))) break;
           tc_fence_after();
           bwd_issue_ss<D, L>(tmem + kS, sQ, sK + (g % RA) * L::kTileBytes, idesc_ss);
           mma_commit(b_s_full);
           ++s_iter;
-          if (!(ok = ATTN_BWD_WAIT(rg.b_full + 8 * (g % RB), (g / RB) & 1, 53))) break;
+          if (!(ok = ATTN_BWD_WAIT_W(rg.b_full + 8 * (g % RB), (g / RB) & 1, 53))) break;
           tc_fence_after();
           bwd_issue_ss<D, L>(tmem + kDP, sDO, sV + (g % RB) * L::kTileBytes, idesc_ss);
           mma_commit(b_dp_full);
@@ -332,16 +334,16 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
           const uint32_t gj = g + j, gn = gj + 1;
           if (j + 1 < nkv) {
             // S_{j+1} may overwrite S once both warpgroups have read S_j
-            if (!(ok = ATTN_BWD_WAIT(rg.a_full + 8 * (gn % RA), (gn / RA) & 1, 54))) break;
-            if (!(ok = ATTN_BWD_WAIT(b_s_free, (s_iter - 1) & 1, 55))) break;
+            if (!(ok = ATTN_BWD_WAIT_W(rg.a_full + 8 * (gn % RA), (gn / RA) & 1, 54))) break;
+            if (!(ok = ATTN_BWD_WAIT_W(b_s_free, (s_iter - 1) & 1, 55))) break;
             tc_fence_after();
             bwd_issue_ss<D, L>(tmem + kS, sQ, sK + (gn % RA) * L::kTileBytes, idesc_ss);
             mma_commit(b_s_full);
             ++s_iter;
           }
-          if (!(ok = ATTN_BWD_WAIT(b_ds_ready, ds_iter & 1, 56))) break;
+          if (!(ok = ATTN_BWD_WAIT_W(b_ds_ready, ds_iter & 1, 56))) break;
           ++ds_iter;
-          if (j == 0 && units > 0 && !(ok = ATTN_BWD_WAIT(b_dq_free, (units - 1) & 1, 57))) break;
+          if (j == 0 && units > 0 && !(ok = ATTN_BWD_WAIT_W(b_dq_free, (units - 1) & 1, 57))) break;
           tc_fence_after();
           bwd_issue_ts<L>(tmem + kDQ, tmem + kDP, sK + (gj % RA) * L::kTileBytes, idesc_dq, j > 0);
           mma_commit(rg.a_empty + 8 * (gj % RA));
@@ -349,7 +351,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             mma_commit(b_dq_done);
           } else {
             // dP_{j+1} overwrites dS_j, which the dQ product above has consumed
-            if (!(ok = ATTN_BWD_WAIT(rg.b_full + 8 * (gn % RB), (gn / RB) & 1, 58))) break;
+            if (!(ok = ATTN_BWD_WAIT_W(rg.b_full + 8 * (gn % RB), (gn / RB) & 1, 58))) break;
             tc_fence_after();
             bwd_issue_ss<D, L>(tmem + kDP, sDO, sV + (gn % RB) * L::kTileBytes, idesc_ss);
             mma_commit(b_dp_full);
@@ -362,7 +364,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       }
       mma_commit(b_drain);
       volatile int no_abort = 0;
-      mbar_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
+      warp_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
     }
   } else {
     // ----------------------------------------------------------- compute
@@ -560,7 +562,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       bwd_producer_drain<RA, RB>(ok, ga, gb, units, rg, b_kv_full, b_kv_empty, abort_flag, tmo, p.err, 73);
     }
   } else if (warp == kBwdMmaWarp) {
-    if (lane == 0) {
+    {  // whole warp, warp-uniform; one elected lane issues each MMA and commit
       constexpr uint32_t idesc_ss = make_idesc(kBlockM, kBlockN, 1, false);
       constexpr uint32_t idesc_acc = make_idesc(kBlockM, D, 1, true);  // B = dO or Q, MN-major
       uint32_t g = 0, p_iter = 0, ds_iter = 0;
@@ -572,13 +574,13 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         int bh, kb, i0;
         unit(u, bh, kb, i0);
         const int n = T - i0;
-        if (!(ok = ATTN_BWD_WAIT(b_kv_full, units & 1, 80))) break;
+        if (!(ok = ATTN_BWD_WAIT_W(b_kv_full, units & 1, 80))) break;
         {  // S^T_0 = K Q_0^T and dP^T_0 = V dO_0^T
-          if (!(ok = ATTN_BWD_WAIT(rg.a_full + 8 * (g % RA), (g / RA) & 1, 81))) break;
+          if (!(ok = ATTN_BWD_WAIT_W(rg.a_full + 8 * (g % RA), (g / RA) & 1, 81))) break;
           tc_fence_after();
           bwd_issue_ss<D, L>(tmem + kS, sK, sQ + (g % RA) * L::kTileBytes, idesc_ss);
           mma_commit(b_st_full);
-          if (!(ok = ATTN_BWD_WAIT(rg.b_full + 8 * (g % RB), (g / RB) & 1, 82))) break;
+          if (!(ok = ATTN_BWD_WAIT_W(rg.b_full + 8 * (g % RB), (g / RB) & 1, 82))) break;
           tc_fence_after();
           bwd_issue_ss<D, L>(tmem + kDP, sV, sDO + (g % RB) * L::kTileBytes, idesc_ss);
           mma_commit(b_dpt_full);
@@ -587,21 +589,21 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         for (int b = 0; b < n && ok; ++b) {
           const uint32_t gb = g + b, gn = gb + 1;
           // dV += P^T dO once both warpgroups have written P^T
-          if (!(ok = ATTN_BWD_WAIT(b_p_ready, p_iter & 1, 83))) break;
+          if (!(ok = ATTN_BWD_WAIT_W(b_p_ready, p_iter & 1, 83))) break;
           ++p_iter;
-          if (b == 0 && units > 0 && !(ok = ATTN_BWD_WAIT(b_acc_free, (units - 1) & 1, 84))) break;
+          if (b == 0 && units > 0 && !(ok = ATTN_BWD_WAIT_W(b_acc_free, (units - 1) & 1, 84))) break;
           tc_fence_after();
           bwd_issue_ts<L>(tmem + kDV, tmem + kS, sDO + (gb % RB) * L::kTileBytes, idesc_acc, b > 0);
           mma_commit(rg.b_empty + 8 * (gb % RB));
           if (b + 1 < n) {
             // S^T_{b+1} overwrites P^T_b, which the dV product above has consumed
-            if (!(ok = ATTN_BWD_WAIT(rg.a_full + 8 * (gn % RA), (gn / RA) & 1, 85))) break;
+            if (!(ok = ATTN_BWD_WAIT_W(rg.a_full + 8 * (gn % RA), (gn / RA) & 1, 85))) break;
             tc_fence_after();
             bwd_issue_ss<D, L>(tmem + kS, sK, sQ + (gn % RA) * L::kTileBytes, idesc_ss);
             mma_commit(b_st_full);
           }
           // dK += dS^T Q once both warpgroups have written dS^T
-          if (!(ok = ATTN_BWD_WAIT(b_ds_ready, ds_iter & 1, 86))) break;
+          if (!(ok = ATTN_BWD_WAIT_W(b_ds_ready, ds_iter & 1, 86))) break;
           ++ds_iter;
           tc_fence_after();
           bwd_issue_ts<L>(tmem + kDK, tmem + kDP, sQ + (gb % RA) * L::kTileBytes, idesc_acc, b > 0);
@@ -610,7 +612,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             mma_commit(b_acc_done);
           } else {
             // dP^T_{b+1} overwrites dS^T_b, which the dK product above has consumed
-            if (!(ok = ATTN_BWD_WAIT(rg.b_full + 8 * (gn % RB), (gn / RB) & 1, 87))) break;
+            if (!(ok = ATTN_BWD_WAIT_W(rg.b_full + 8 * (gn % RB), (gn / RB) & 1, 87))) break;
             tc_fence_after();
             bwd_issue_ss<D, L>(tmem + kDP, sV, sDO + (gn % RB) * L::kTileBytes, idesc_ss);
             mma_commit(b_dpt_full);
@@ -622,7 +624,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       }
       mma_commit(b_drain);
       volatile int no_abort = 0;
-      mbar_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
+      warp_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
     }
   } else {
     // ----------------------------------------------------------- compute

@@ -387,8 +387,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           mbar_wait(b_v_full + 8 * (i % NV), (i / NV) & 1, &no_abort, tmo, nullptr, 0);
         if (q_issued > 0) mbar_wait(b_q_full, (q_issued - 1) & 1, &no_abort, tmo, nullptr, 0);
       }
-    } else if (warp == kMmaWarp && lane == 0) {
+    } else if (warp == kMmaWarp) {
       // ---------------------------------------------------------------- MMA
+      // The whole warp runs this role in warp-uniform control flow; one elected
+      // lane issues each MMA and commit.
       // S: bf16 (kind::f16, format 1) or e4m3 (kind::f8f6f4, format 0).
       // P V: kind::f16 with bf16 (BF16 path) or f16 (FP8 path: format 0) operands.
       constexpr uint32_t idesc_s = make_idesc(kBlockM, kBlockN, kFp8 ? 0u : 1u, false);
@@ -444,10 +446,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const UnitInfo ui = unit_info(u, p);
         const int n0 = ui.n[0], n1 = ui.n[1];
         if (n1 == 0) continue;
-        if (!(ok = mbar_wait(b_q_full, units & 1, abort_flag, tmo, p.err, 10))) break;
+        if (!(ok = warp_wait(b_q_full, units & 1, abort_flag, tmo, p.err, 10))) break;
         {
           const uint32_t sk = g % NK;
-          if (!(ok = mbar_wait(b_k_full + 8 * sk, (g / NK) & 1, abort_flag, tmo, p.err, 11))) break;
+          if (!(ok = warp_wait(b_k_full + 8 * sk, (g / NK) & 1, abort_flag, tmo, p.err, 11))) break;
           tc_fence_after();
           if (n0 > 0) issue_s(0, sk);
           issue_s(1, sk);
@@ -475,13 +477,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           for (int t = 0; t < kTilesPerUnit; ++t) {
             const int nt = t == 0 ? n0 : n1;
             if (j >= nt || !ok) continue;
-            if (!(ok = mbar_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
+            if (!(ok = warp_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
             ++p_iter[t];
-            if (!(ok = mbar_wait(v_bar, v_par, abort_flag, tmo, p.err, 14))) break;
+            if (!(ok = warp_wait(v_bar, v_par, abort_flag, tmo, p.err, 14))) break;
             if (j == 0) {
               // O_t is overwritten: the epilogue of its previous unit must have read it
               if (o_uses[t] > 0 &&
-                  !(ok = mbar_wait(b_o_free + 8 * t, (o_uses[t] - 1) & 1, abort_flag, tmo, p.err, 15 + t)))
+                  !(ok = warp_wait(b_o_free + 8 * t, (o_uses[t] - 1) & 1, abort_flag, tmo, p.err, 15 + t)))
                 break;
               ++o_uses[t];
             }
@@ -494,7 +496,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
               else mma_commit(b_v_empty + 8 * (gj % NV));
             }
             if (j + 1 < nt) {
-              if (!(ok = mbar_wait(b_k_full + 8 * skn, phkn, abort_flag, tmo, p.err, 17))) break;
+              if (!(ok = warp_wait(b_k_full + 8 * skn, phkn, abort_flag, tmo, p.err, 17))) break;
               tc_fence_after();
               issue_s(t, skn);
               if (t == 1) {
@@ -510,7 +512,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       // Every MMA issued has completed before TMEM is released.
       mma_commit(b_drain);
       volatile int no_abort = 0;
-      mbar_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
+      warp_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
     } else if (Plan::kNumConv > 0 && warp >= kConvertWarp0) {
       // ------------------------------------------------- FP8: V e4m3 -> f16
       // Each thread converts 16 of the 1024 16-byte units of a V block (128 key
