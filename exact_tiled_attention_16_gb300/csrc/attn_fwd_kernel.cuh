@@ -474,12 +474,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             v_bar = b_v_full + 8 * (gj % NV);
             v_par = (gj / NV) & 1;
           }
+          // Operands that arrived long ago are checked first, off the path from a
+          // ready P to its P V product: V_j (both tiles) and K_{j+1} (next Q K^T).
+          if (!(ok = warp_wait(v_bar, v_par, abort_flag, tmo, p.err, 14))) break;
+          if (j + 1 < n1 && !(ok = warp_wait(b_k_full + 8 * skn, phkn, abort_flag, tmo, p.err, 17))) break;
           for (int t = 0; t < kTilesPerUnit; ++t) {
             const int nt = t == 0 ? n0 : n1;
             if (j >= nt || !ok) continue;
-            if (!(ok = warp_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
-            ++p_iter[t];
-            if (!(ok = warp_wait(v_bar, v_par, abort_flag, tmo, p.err, 14))) break;
             if (j == 0) {
               // O_t is overwritten: the epilogue of its previous unit must have read it
               if (o_uses[t] > 0 &&
@@ -487,20 +488,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 break;
               ++o_uses[t];
             }
+            if (!(ok = warp_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
+            ++p_iter[t];
             tc_fence_after();
             issue_pv(t, v_base, j > 0);
+            if (j + 1 < nt) issue_s(t, skn);
             if (j == nt - 1) mma_commit(b_pv_done + 8 * t);
             if (t == 1) {
-              // tile 1 is the last user of V_j
+              // tile 1 is the last user of V_j and K_{j+1}
               if constexpr (Plan::kNumConv > 0) mma_commit(b_c_empty + 8 * (gj & 1));
               else mma_commit(b_v_empty + 8 * (gj % NV));
-            }
-            if (j + 1 < nt) {
-              if (!(ok = warp_wait(b_k_full + 8 * skn, phkn, abort_flag, tmo, p.err, 17))) break;
-              tc_fence_after();
-              issue_s(t, skn);
-              if (t == 1) {
-                mma_commit(b_k_empty + 8 * skn);  // tile 1 is the last user of K_{j+1}
+              if (j + 1 < nt) {
+                mma_commit(b_k_empty + 8 * skn);
                 if (j + 1 == n1 - 1) mma_commit(b_q_empty);
               }
             }
