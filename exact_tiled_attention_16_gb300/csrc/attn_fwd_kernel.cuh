@@ -148,7 +148,7 @@ struct SmemPlan {
   static constexpr uint32_t kV = kK + NK * In::kTileBytes;
   static constexpr uint32_t kC = kV + NV * kVTileBytes;
   static constexpr uint32_t kBars = kC + kNumConv * V16::kTileBytes;
-  static constexpr int kNumBars = 12 + 2 * NK + 2 * NV + 2 * kNumConv;
+  static constexpr int kNumBars = 14 + 2 * NK + 2 * NV + 2 * kNumConv;
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBars + 8 * kNumBars + 16;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
@@ -277,6 +277,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const uint32_t b_v_empty = smem_u32(&bars[12 + 2 * NK + NV]);
   const uint32_t b_c_full = smem_u32(&bars[12 + 2 * NK + 2 * NV]);  // + 8 b (FP8)
   const uint32_t b_c_empty = b_c_full + 8 * Plan::kNumConv;
+  const uint32_t b_pa_full = b_c_empty + 8 * Plan::kNumConv;  // + 8 t: first half of P_t written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[Plan::kNumBars]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -293,6 +294,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       mbar_init(b_p_full + 8 * t, 128);
       mbar_init(b_pv_done + 8 * t, 1);
       mbar_init(b_o_free + 8 * t, 128);
+      mbar_init(b_pa_full + 8 * t, 128);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(b_k_full + 8 * s, 1);
@@ -420,7 +422,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       // O_t (+)= P_t V with the 16-bit V tile at v_base: P_t from TMEM (two keys
       // per column), V MN-major, 16 key rows of 128 bytes per step, column chunks
       // kChunkBytes apart.
-      auto issue_pv = [&](int t, uint32_t v_base, bool accumulate) {
+      // (16-bit P) `half` selects the keys: 0 = 0..63, 1 = 64..127, -1 = all.
+      auto issue_pv = [&](int t, uint32_t v_base, bool accumulate, int half) {
         if constexpr (kFp4) {
           // P_t (e2m1, S_t columns 0..15) x V^T (K-major, 64-byte swizzle): two
           // K = 64 steps of 32 bytes; scale words of P and V in S_t's columns too
@@ -432,10 +435,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         } else {
           const uint32_t vb0 = sdesc_lo(v_base, LV::kChunkBytes);
           constexpr uint32_t hi = sdesc_hi_sw128(1024);
+          const int kk0 = half == 1 ? kBlockN / 32 : 0;
+          const int kk1 = half == 0 ? kBlockN / 32 : kBlockN / 16;
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_f16_ts_w(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8, vb0 + ((kk * 16 * 128) >> 4), hi, idesc_o,
-                         (accumulate || kk > 0) ? 1u : 0u);
+            if (kk >= kk0 && kk < kk1)
+              mma_f16_ts_w(tmem + kTmemO[t], tmem + kTmemS[t] + kk * 8, vb0 + ((kk * 16 * 128) >> 4), hi, idesc_o,
+                           (accumulate || kk > 0) ? 1u : 0u);
         }
       };
       int o_uses[2] = {0, 0};  // units in which tile t has written O_t
@@ -488,10 +494,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 break;
               ++o_uses[t];
             }
+            if constexpr (!kFp4) {
+              // the first half of P_t is written before the second is computed, so
+              // its half of P V runs while the softmax works on the rest
+              if (!(ok = warp_wait(b_pa_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 18 + t))) break;
+              tc_fence_after();
+              issue_pv(t, v_base, j > 0, 0);
+            }
             if (!(ok = warp_wait(b_p_full + 8 * t, p_iter[t] & 1, abort_flag, tmo, p.err, 12 + t))) break;
             ++p_iter[t];
             tc_fence_after();
-            issue_pv(t, v_base, j > 0);
+            if constexpr (kFp4) issue_pv(t, v_base, j > 0, -1);
+            else issue_pv(t, v_base, true, 1);
             if (j + 1 < nt) issue_s(t, skn);
             if (j == nt - 1) mma_commit(b_pv_done + 8 * t);
             if (t == 1) {
@@ -754,6 +768,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           const float m_sub = ((m_use == -INFINITY) ? 0.f : m_use) - off;
           float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                            make_float2(0.f, 0.f)};
+          // In two halves of 64 keys: the first half of P is stored and announced
+          // (pa_full) before the second is computed, so that its half of P V runs
+          // meanwhile.
           uint32_t pk[kBlockN / 2];
 #pragma unroll
           for (int c = 0; c < kBlockN; c += 2) {
@@ -762,6 +779,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
             if constexpr (kFp8) pk[c / 2] = pack_f16x2(e.x, e.y);
             else pk[c / 2] = pack_bf16x2(e.x, e.y);
+            if (c == kBlockN / 2 - 2) {
+              tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(b_pa_full + 8 * t);
+            }
           }
           const float2 acc01 = fadd2(acc[0], acc[1]);
           const float2 acc23 = fadd2(acc[2], acc[3]);
@@ -769,7 +792,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           float rowsum = accs.x + accs.y;
           if constexpr (kFp8) rowsum *= ex2_approx(-off);  // back to the unscaled P
           l = l * alpha + rowsum;
-          tmem_st64(tS, pk);
+          tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
         }
         tmem_st_wait();
         tc_fence_before();
