@@ -218,8 +218,9 @@ int validate_tensors(const void* q, const void* k, const void* v, const void* o,
   return ATTN_OK;
 }
 
+// kv_key_bytes: bytes of one key's K and V rows together (sizes the L2 test below)
 void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset, int k_offset, int num_splits,
-                 float scale, int dev) {
+                 float scale, int dev, long long kv_key_bytes) {
   std::memset(&p, 0, sizeof(p));
   p.BH = BH;
   p.Nq = Nq;
@@ -238,7 +239,16 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
   // CTAs; with fewer than four rounds of them the last, partly empty round costs
   // more than the balance gains
   const long long combined = static_cast<long long>(BH) * ((p.num_pairs + 1) / 2);
-  p.zigzag = (causal && p.num_splits == 1 && combined >= 4ll * g_dev[dev].num_sms) ? 1 : 0;
+  p.order = kOrderHeads;
+  if (causal && p.num_splits == 1) {
+    if (combined >= 4ll * g_dev[dev].num_sms) {
+      p.order = kOrderZigzag;
+    } else if (static_cast<long long>(BH) * Nk * kv_key_bytes <= kPairOrderMaxKvBytes) {
+      // few rounds: deal the units heaviest first across all heads (near-optimal
+      // balance); every head's K/V stays in L2 since all of them fit
+      p.order = kOrderPairs;
+    }
+  }
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
   p.err = g_dev[dev].err_ptr;
@@ -248,7 +258,7 @@ template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const FwdParams& p, int dev,
            void* stream) {
   // work items dealt to CTAs: units, or combined heavy+light pairs under zigzag
-  const int items = p.zigzag ? p.BH * ((p.num_pairs + 1) / 2) : p.num_units;
+  const int items = p.order == kOrderZigzag ? p.BH * ((p.num_pairs + 1) / 2) : p.num_units;
   const int grid = items < g_dev[dev].num_sms ? items : g_dev[dev].num_sms;
   attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4>
       <<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8, kFp4>::kBytes, static_cast<cudaStream_t>(stream)>>>(mq, mk,
@@ -335,7 +345,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, B * H, N, N, causal, 0, 0, 1, scale, dev);
+  fill_params(p, B * H, N, N, causal, 0, 0, 1, scale, dev, 4ll * d);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   return launch_bf16(q, k, v, d, false, p, dev, stream);
@@ -388,7 +398,7 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
     if (c >= kHostSlots) ck(cudaStreamWaitEvent(sc, hp.out_done[slot], 0));
     if (!ok) break;
     FwdParams p;
-    fill_params(p, hn, N, N, causal, 0, 0, 1, scale, dev);
+    fill_params(p, hn, N, N, causal, 0, 0, 1, scale, dev, 4ll * d);
     p.o = reinterpret_cast<__nv_bfloat16*>(dout);
     p.lse = lse ? dl : nullptr;
     if ((rc = launch_bf16(dq, dk, dv, d, false, p, dev, sc)) != ATTN_OK) return rc;
@@ -425,7 +435,7 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map(&mv, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev);
+  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev, 2ll * d);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.q_scale = q_scale;
@@ -455,7 +465,7 @@ int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* 
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map_vt4(&mv, vt4, d, N, BH)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev);
+  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev, 2ll * d);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.q_scale = q_scale;
@@ -473,7 +483,7 @@ int attn_fwd_partial(const void* q, const void* k, const void* v, float* o_part,
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, B * H, Nq, Nk, causal, q_offset, k_offset, 1, scale, dev);
+  fill_params(p, B * H, Nq, Nk, causal, q_offset, k_offset, 1, scale, dev, 4ll * d);
   p.o_part = o_part;
   p.lse_part = lse_part;
   return launch_bf16(q, k, v, d, true, p, dev, stream);
@@ -518,7 +528,7 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
   const int BH = B * H;
   FwdParams p;
   // causal: the queries are the last Nq positions of the Nk keys
-  fill_params(p, BH, Nq, Nk, causal, Nk - Nq, 0, num_splits, scale, dev);
+  fill_params(p, BH, Nq, Nk, causal, Nk - Nq, 0, num_splits, scale, dev, 4ll * d);
   const long long S = p.num_splits;
   if (workspace_bytes < splitkv_workspace_bytes(BH, Nq, d, S)) return ATTN_ERR_DIMS;
   const long long rows = static_cast<long long>(BH) * Nq;

@@ -112,7 +112,7 @@ struct FwdParams {
   int blocks_per_split;
   int num_units;      // BH * num_pairs * num_splits
   int causal;
-  int zigzag;         // causal, unsplit: balanced heavy+light pairing of units
+  int order;          // unit order: kOrderHeads, kOrderZigzag or kOrderPairs (below)
   float scale_log2;   // scale * log2(e)
   const float* q_scale;  // FP8 only: [B*H, num_kblocks] block scales
   const float* k_scale;
@@ -153,10 +153,19 @@ struct SmemPlan {
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
-// Run order: head-major (units of one head are adjacent, so concurrently running
-// units share K/V in L2); under the causal mask each head's pairs run from the
-// heaviest (last rows) to the lightest; the key-range splits of a pair are
-// adjacent.
+// Run order (FwdParams::order):
+//   kOrderHeads   head-major: the units of a head are adjacent, so concurrently
+//                 running units share K/V in L2; under the causal mask each head's
+//                 pairs run from the heaviest (last rows) to the lightest; the
+//                 key-range splits of a pair are adjacent.
+//   kOrderZigzag  causal with many units: heavy+light pairs combined, head-major
+//                 (see unit_for_round).
+//   kOrderPairs   causal with few rounds and every head's K/V small enough to stay
+//                 in L2 together: pair-major, heaviest first, dealt back and forth
+//                 over the CTAs -- close to longest-job-first balance (e.g. 94%
+//                 against 84% for 64 heads of 2048 keys on 152 SMs).
+constexpr int kOrderHeads = 0, kOrderZigzag = 1, kOrderPairs = 2;
+constexpr long long kPairOrderMaxKvBytes = 64ll << 20;
 struct UnitInfo {
   int bh, pair, split;
   int kb0;   // first K/V block of the unit's key range
@@ -165,12 +174,20 @@ struct UnitInfo {
 
 __device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p) {
   UnitInfo ui;
-  const int per_head = p.num_pairs * p.num_splits;
-  ui.bh = u / per_head;
-  const int r = u - ui.bh * per_head;
-  const int pr = r / p.num_splits;
-  ui.split = r - pr * p.num_splits;
-  ui.pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
+  if (p.order == kOrderPairs) {
+    // causal, unsplit: all heads' heaviest pair, then all heads' next, ...
+    const int pr = u / p.BH;
+    ui.bh = u - pr * p.BH;
+    ui.split = 0;
+    ui.pair = p.num_pairs - 1 - pr;
+  } else {
+    const int per_head = p.num_pairs * p.num_splits;
+    ui.bh = u / per_head;
+    const int r = u - ui.bh * per_head;
+    const int pr = r / p.num_splits;
+    ui.split = r - pr * p.num_splits;
+    ui.pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
+  }
   ui.kb0 = ui.split * p.blocks_per_split;
   int kb_end = ui.kb0 + p.blocks_per_split;
   if (kb_end > p.num_kblocks) kb_end = p.num_kblocks;
@@ -207,7 +224,7 @@ constexpr int kSkipRound = -2;
 __device__ __forceinline__ int unit_for_round(int round, const FwdParams& p) {
   const int G = gridDim.x;
   const int c = blockIdx.x;
-  if (p.zigzag) {
+  if (p.order == kOrderZigzag) {
     const int half = (p.num_pairs + 1) >> 1;
     const int k = (round >> 1) * G + c;
     if (k >= p.BH * half) return kNoMoreUnits;

@@ -204,3 +204,24 @@ def test_zigzag_schedule_covers_every_unit(shape):
     assert not torch.isnan(o.float()).any() and not torch.isnan(lse).any()
     assert_bf16_tol(compare_rows(w, o.float().cpu().numpy().astype(np.float64),
                                  lse.cpu().numpy().astype(np.float64)), f"zigzag {shape}")
+
+
+@pytest.mark.parametrize("shape", [(2, 76, 640, 128), (3, 50, 1024, 64), (1, 7, 2304, 128)],
+                         ids=["pairs3_odd_3rounds", "pairs4_d64", "few_heads_ragged_rounds"])
+def test_pair_order_schedule_covers_every_unit(shape):
+    """Causal launches with fewer than four rounds of combined units and every
+    head's K/V small enough for L2 take the pair-major order (all heads'
+    heaviest pair first, dealt back and forth over the CTAs); every row must be
+    written and correct, including heads whose pairs land on different CTAs in
+    different rounds."""
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d = shape
+    w = synth.make_bf16(B, H, N, d, True, seed=91 + N)
+    q, k, v = to_device(w)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    pkg.attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o.float()).any() and not torch.isnan(lse).any()
+    assert_bf16_tol(compare_rows(w, o.float().cpu().numpy().astype(np.float64),
+                                 lse.cpu().numpy().astype(np.float64)), f"pair order {shape}")
