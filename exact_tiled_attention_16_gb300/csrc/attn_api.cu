@@ -326,7 +326,9 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   if (pblocks > cap) pblocks = cap;
   attn_bwd_prep_kernel<D><<<static_cast<int>(pblocks), 256, 0, st>>>(bp);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-  const int grid = bp.num_units < g_dev[dev].num_sms ? bp.num_units : g_dev[dev].num_sms;
+  // CTAs: units, or block pairs under the zigzag order
+  const int items = bp.order == kBwdOrderZigzag ? bp.BH * ((bp.num_blocks + 1) / 2) : bp.num_units;
+  const int grid = items < g_dev[dev].num_sms ? items : g_dev[dev].num_sms;
   const size_t smem = BwdSmem<D, RA, RB>::kBytes;
   attn_bwd_dq_kernel<D, RA, RB><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
@@ -590,6 +592,14 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   bp.N = N;
   bp.num_units = BH * bp.num_blocks;
   bp.causal = causal ? 1 : 0;
+  bp.order = kBwdOrderHeads;
+  if (causal) {
+    // both passes stream two tensors of d bf16 per key per head (K, V or Q, dO)
+    const long long streamed = static_cast<long long>(BH) * bp.Npad * 4ll * d;
+    if (streamed <= kPairOrderMaxKvBytes) bp.order = kBwdOrderBlocks;
+    else if (static_cast<long long>(BH) * ((bp.num_blocks + 1) / 2) >= 4ll * g_dev[dev].num_sms)
+      bp.order = kBwdOrderZigzag;
+  }
   bp.scale = scale;
   bp.scale_log2 = scale * 1.4426950408889634f;
   bp.timeout_ns = g_timeout_ns;

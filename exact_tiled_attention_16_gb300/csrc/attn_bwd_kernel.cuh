@@ -52,6 +52,7 @@ struct BwdParams {
   int BH, N, Npad;            // Npad = 128 * num_blocks
   int num_blocks;             // ceil(N / 128)
   int num_units;              // BH * num_blocks
+  int order;                  // unit order: kBwdOrderHeads, kBwdOrderZigzag or kBwdOrderBlocks
   int causal;
   float scale;
   float scale_log2;           // scale * log2(e)
@@ -186,6 +187,60 @@ __device__ __forceinline__ void bwd_producer_drain(bool ok, uint32_t ga, uint32_
   }
 }
 
+// Unit order of both passes.  A unit is (bh, rank r) with r = 0 the heaviest block
+// of a head under the causal mask (dq: the last query block; dkdv: the first key
+// block); without the mask all blocks cost the same.
+//   kBwdOrderHeads   head-major, heaviest first, dealt over the CTAs in a snake
+//                    (mirror on odd rounds): the units of a head run together and
+//                    share its streamed tensors in L2.
+//   kBwdOrderZigzag  causal with at least four rounds of pairs: block pairs
+//                    (r, T-1-r) of one head cost the same for every r; CTA k of a
+//                    round takes pair k's heavy block in even iterations and its
+//                    light one in odd iterations (an odd T leaves the middle block
+//                    alone), head-major.
+//   kBwdOrderBlocks  causal with fewer rounds and all heads' streamed tensors within
+//                    L2: block-major, heaviest first over all heads, in the snake
+//                    (~98% balance where head-major gives ~85%).
+constexpr int kBwdOrderHeads = 0, kBwdOrderZigzag = 1, kBwdOrderBlocks = 2;
+constexpr int kBwdDone = -1, kBwdSkip = -2;
+struct BwdUnit {
+  int status;  // 0, kBwdDone or kBwdSkip
+  int bh, r;
+};
+__device__ __forceinline__ BwdUnit bwd_unit_for_round(int round, const BwdParams& p) {
+  const int G = gridDim.x, c = blockIdx.x, T = p.num_blocks;
+  BwdUnit u{0, 0, 0};
+  if (p.order == kBwdOrderZigzag) {
+    const int half = (T + 1) >> 1;
+    const int k = (round >> 1) * G + c;
+    if (k >= p.BH * half) {
+      u.status = kBwdDone;
+      return u;
+    }
+    u.bh = k / half;
+    const int cc = k - u.bh * half;
+    if ((round & 1) && T - 1 - cc == cc) {
+      u.status = kBwdSkip;
+      return u;
+    }
+    u.r = (round & 1) ? T - 1 - cc : cc;
+    return u;
+  }
+  const int pos = round * G + ((round & 1) ? (G - 1 - c) : c);
+  if (pos >= p.num_units) {
+    u.status = kBwdDone;
+    return u;
+  }
+  if (p.order == kBwdOrderBlocks) {
+    u.r = pos / p.BH;
+    u.bh = pos - u.r * p.BH;
+  } else {
+    u.bh = pos / T;
+    u.r = pos - u.bh * T;
+  }
+  return u;
+}
+
 // Bounded wait + abort plumbing shared by the two passes
 #define ATTN_BWD_WAIT(bar, par, where) mbar_wait((bar), (par), abort_flag, tmo, p.err, (where))
 // the same, taken by a whole warp (same answer on every lane)
@@ -254,16 +309,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const uint32_t tmem = *tmem_slot;
 
   // unit -> (bh, query block qb); causal: heaviest (last) query blocks first
-  auto unit = [&](int u, int& bh, int& qb, int& nkv) {
-    bh = u / T;
-    const int r = u - bh * T;
-    qb = p.causal ? (T - 1 - r) : r;
+  auto unit = [&](const BwdUnit& uu, int& bh, int& qb, int& nkv) {
+    bh = uu.bh;
+    qb = p.causal ? (T - 1 - uu.r) : uu.r;
     nkv = p.causal ? qb + 1 : T;
-  };
-  auto unit_for_round = [&](int round) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int pos = round * G + ((round & 1) ? (G - 1 - c) : c);
-    return pos < p.num_units ? pos : -1;
   };
 
   if (warp == kBwdProducerWarp) {
@@ -274,8 +323,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       int units = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round);
-        if (u < 0) break;
+        const BwdUnit u = bwd_unit_for_round(round, p);
+        if (u.status == kBwdDone) break;
+        if (u.status == kBwdSkip) continue;
         int bh, qb, nkv;
         unit(u, bh, qb, nkv);
         if (units > 0 && !(ok = ATTN_BWD_WAIT(b_qd_empty, (units - 1) & 1, 40))) break;
@@ -311,8 +361,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       int units = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round);
-        if (u < 0) break;
+        const BwdUnit u = bwd_unit_for_round(round, p);
+        if (u.status == kBwdDone) break;
+        if (u.status == kBwdSkip) continue;
         int bh, qb, nkv;
         unit(u, bh, qb, nkv);
         if (!(ok = ATTN_BWD_WAIT_W(b_qd_full, units & 1, 50))) break;
@@ -378,8 +429,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     int units = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
-      const int u = unit_for_round(round);
-      if (u < 0) break;
+      const BwdUnit u = bwd_unit_for_round(round, p);
+      if (u.status == kBwdDone) break;
+      if (u.status == kBwdSkip) continue;
       int bh, qb, nkv;
       unit(u, bh, qb, nkv);
       const int row = qb * kBlockM + t;
@@ -513,15 +565,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 
   // unit -> (bh, key block kb); query blocks i0 .. T-1 (causal: i0 = kb, so the
   // first key blocks are the heaviest and run first)
-  auto unit = [&](int u, int& bh, int& kb, int& i0) {
-    bh = u / T;
-    kb = u - bh * T;
+  auto unit = [&](const BwdUnit& uu, int& bh, int& kb, int& i0) {
+    bh = uu.bh;
+    kb = uu.r;
     i0 = p.causal ? kb : 0;
-  };
-  auto unit_for_round = [&](int round) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int pos = round * G + ((round & 1) ? (G - 1 - c) : c);
-    return pos < p.num_units ? pos : -1;
   };
 
   if (warp == kBwdProducerWarp) {
@@ -532,8 +579,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       int units = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round);
-        if (u < 0) break;
+        const BwdUnit u = bwd_unit_for_round(round, p);
+        if (u.status == kBwdDone) break;
+        if (u.status == kBwdSkip) continue;
         int bh, kb, i0;
         unit(u, bh, kb, i0);
         if (units > 0 && !(ok = ATTN_BWD_WAIT(b_kv_empty, (units - 1) & 1, 70))) break;
@@ -569,8 +617,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       int units = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round);
-        if (u < 0) break;
+        const BwdUnit u = bwd_unit_for_round(round, p);
+        if (u.status == kBwdDone) break;
+        if (u.status == kBwdSkip) continue;
         int bh, kb, i0;
         unit(u, bh, kb, i0);
         const int n = T - i0;
@@ -638,8 +687,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     int units = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
-      const int u = unit_for_round(round);
-      if (u < 0) break;
+      const BwdUnit u = bwd_unit_for_round(round, p);
+      if (u.status == kBwdDone) break;
+      if (u.status == kBwdSkip) continue;
       int bh, kb, i0;
       unit(u, bh, kb, i0);
       const int key = kb * kBlockN + t;

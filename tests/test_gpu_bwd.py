@@ -95,6 +95,17 @@ def test_many_units_per_cta(shape, causal):
     check_heads(w, do_bits, got, heads=[heads[i] for i in pick] + [heads[-1]])
 
 
+def test_zigzag_order_odd_blocks():
+    """Causal with many block pairs and streamed tensors beyond the L2 budget: both
+    passes take the zigzag order; an odd block count (33) leaves each head's middle
+    block alone in an odd iteration, which every role must skip alike."""
+    B, H, N, d = 1, 64, 4224, 64
+    w = synth.make_bf16(B, H, N, d, True, seed=4224)
+    do_bits = synth.make_grad_out(B, H, N, d, seed=4224)
+    got = run_bwd(w, do_bits)
+    check_heads(w, do_bits, got, heads=[(0, 0), (0, 31), (0, 63)])
+
+
 @pytest.mark.parametrize("name", ["cfg2n", "cfg2c"])
 def test_cfg2_heads(name):
     w = synth.make_config(name)
