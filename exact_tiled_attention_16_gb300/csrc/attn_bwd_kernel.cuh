@@ -21,7 +21,7 @@
 // Each CTA: warps 0-7 compute in two warpgroups -- thread t of warpgroup h owns
 // TMEM lane t (one row of the tile) and columns 64h..64h+63 of each 128-column
 // tile, and writes its bf16 result into the first 32 of those columns -- warp 8
-// is the TMA producer, warp 9 the single-thread MMA issuer (and TMEM owner).
+// is the TMA producer, warp 9 the MMA warp (one elected lane issues; TMEM owner).
 // dQ and dK/dV are separate passes, so no atomics are needed and the result is
 // deterministic (the two S-type products are computed in both passes).
 #pragma once

@@ -17,7 +17,7 @@
 //   warps 4-7   softmax of tile 1
 //   warp  8     producer: TMA loads of the two Q tiles and of the K and V
 //               blocks into two rings of shared-memory stages
-//   warp  9     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//   warp  9     MMA warp (one elected lane issues): S_t = Q_t K_j^T, O_t += P_t V_j
 //   warps 10-11 FP8 only: convert each e4m3 V block to f16 in shared memory
 // The MMA warp interleaves the tiles -- P0 V_j, S0 = Q0 K_{j+1}^T, P1 V_j,
 // S1 = Q1 K_{j+1}^T -- so that the softmax of one tile runs while the tensor
@@ -37,7 +37,9 @@
 //   c_full/c_empty[b]     FP8: f16 copy of V (converter -> MMA -> converter)
 //   s_full[t]   MMA -> softmax: S_t,j ready; since it is committed after
 //               O_t += P_t,j-1 V_j-1, it also means O_t and P_t are free
-//   p_full[t]   softmax -> MMA: P_t,j written (and O_t rescaled if needed)
+//   pa_full[t]  softmax -> MMA: the first half of P_t,j (keys 0-63) written (and
+//               O_t rescaled if needed); its half of P V may start
+//   p_full[t]   softmax -> MMA: all of P_t,j written
 //   pv_done[t]  MMA -> softmax: the unit's last P_t V product has completed
 //   o_free[t]   softmax -> MMA: the epilogue has read O_t
 //
