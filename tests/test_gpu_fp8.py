@@ -33,6 +33,18 @@ def test_fp8_small_full_oracle(shape, causal):
     assert_fp8_tol(compare_rows(w, o, lse, excess=True), f"fp8 {shape} causal={causal}")
 
 
+@pytest.mark.parametrize("shape", [(2, 40, 1024), (1, 76, 2304)], ids=["pairs4_2rounds", "pairs9_odd_5rounds"])
+def test_fp8_causal_many_units(shape):
+    """Causal FP8 with more units than SMs and every head's K/V within the L2
+    budget: the pair-major order, with the converter warps' buffers and every ring
+    reused across units; sampled rows of every head checked."""
+    B, H, N = shape
+    w = synth.make_fp8(B, H, N, 128, True, seed=500 + N)
+    o, lse = run_fp8(w)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert_fp8_tol(compare_rows(w, o, lse, rows_per_head=64, excess=True), f"fp8 causal {shape}")
+
+
 def test_fp8_no_outliers_no_rotation():
     w = synth.make_fp8(1, 2, 640, 128, False, seed=7, outlier_frac=0.0, rotate=False)
     o, lse = run_fp8(w)

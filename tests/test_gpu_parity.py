@@ -206,8 +206,8 @@ def test_zigzag_schedule_covers_every_unit(shape):
                                  lse.cpu().numpy().astype(np.float64)), f"zigzag {shape}")
 
 
-@pytest.mark.parametrize("shape", [(2, 76, 640, 128), (3, 50, 1024, 64), (1, 7, 2304, 128)],
-                         ids=["pairs3_odd_3rounds", "pairs4_d64", "few_heads_ragged_rounds"])
+@pytest.mark.parametrize("shape", [(2, 76, 640, 128), (3, 50, 1024, 64), (1, 7, 2304, 128), (2, 40, 777, 64)],
+                         ids=["pairs3_odd_3rounds", "pairs4_d64", "few_heads_ragged_rounds", "ragged_tail_d64"])
 def test_pair_order_schedule_covers_every_unit(shape):
     """Causal launches with fewer than four rounds of combined units and every
     head's K/V small enough for L2 take the pair-major order (all heads'
