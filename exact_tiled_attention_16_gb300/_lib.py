@@ -15,7 +15,20 @@ LIB_PATH = os.path.join(_PKG, "libattn.so")
 
 ATTN_OK = 0
 ATTN_BF16 = 0
+# attn_status codes (include/attn.h)
+ATTN_ERR_NULL = -1
+ATTN_ERR_DIMS = -2
+ATTN_ERR_UNSUPPORTED_HEADDIM = -3
+ATTN_ERR_DTYPE = -4
+ATTN_ERR_ALIGN = -5
+ATTN_ERR_OVERFLOW = -6
+ATTN_ERR_LAUNCH = -7
 ATTN_ERR_TIMEOUT = -8
+ATTN_ERR_ARCH = -9
+ATTN_ERR_SCALE = -10
+ATTN_ERR_CUDA = -11
+ATTN_ERR_SCRATCH = -12
+ATTN_ERR_WORKSPACE = -13
 
 _lib = None
 
@@ -66,6 +79,10 @@ def load_library():
     lib.attn_set_wait_timeout_ns.restype = ci
     lib.attn_selftest_wait_timeout.argtypes = [vp]
     lib.attn_selftest_wait_timeout.restype = ci
+    lib.attn_measure_exp2_rates.argtypes = [ctypes.POINTER(cf), ctypes.POINTER(cf), vp]
+    lib.attn_measure_exp2_rates.restype = ci
+    lib.attn_eval_exp2.argtypes = [vp, vp, vp, ctypes.c_longlong, vp]
+    lib.attn_eval_exp2.restype = ci
     _lib = lib
     return lib
 
@@ -402,3 +419,28 @@ def set_wait_timeout_ns(ns: int) -> int:
 
 def selftest_wait_timeout(stream=None) -> int:
     return load_library().attn_selftest_wait_timeout(_stream_handle(stream) or None)
+
+
+def measure_exp2_rates(stream=None):
+    """(ex2 per SM clock per SM on the special-function unit, FMA-pipe polynomial
+    exponentials per SM clock per SM), measured on the current device."""
+    a, b = ctypes.c_float(0.0), ctypes.c_float(0.0)
+    rc = load_library().attn_measure_exp2_rates(ctypes.byref(a), ctypes.byref(b), _stream_handle(stream) or None)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_measure_exp2_rates")
+    return float(a.value), float(b.value)
+
+
+def eval_exp2(x, stream=None):
+    """(y_poly, y_sfu) for a CUDA float32 tensor x: the FMA-pipe polynomial
+    exponential and ex2.approx, evaluated by the library's device code."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    y_poly = torch.empty_like(x)
+    y_sfu = torch.empty_like(x)
+    rc = load_library().attn_eval_exp2(x.data_ptr(), y_poly.data_ptr(), y_sfu.data_ptr(), x.numel(),
+                                       _stream_handle(stream) or None)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_eval_exp2")
+    return y_poly, y_sfu

@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", os.path.join(ROOT, "include")]
-UNITS = ["attn_api.cu"]
+UNITS = ["attn_api.cu", "attn_diag.cu"]
 
 
 def nvcc() -> str:

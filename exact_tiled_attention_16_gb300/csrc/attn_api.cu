@@ -218,6 +218,22 @@ int validate_tensors(const void* q, const void* k, const void* v, const void* o,
   return ATTN_OK;
 }
 
+// Key-range splits a split-K/V launch actually uses for `requested` splits over
+// num_kblocks key blocks: ranges of ceil(num_kblocks / requested) blocks, so
+// there may be fewer ranges than requested (never more than key blocks).
+struct SplitPlan {
+  int blocks_per_split;
+  int num_splits;
+};
+SplitPlan split_plan(int num_kblocks, int requested) {
+  if (requested > num_kblocks) requested = num_kblocks;
+  if (requested < 1) requested = 1;
+  SplitPlan sp;
+  sp.blocks_per_split = (num_kblocks + requested - 1) / requested;
+  sp.num_splits = (num_kblocks + sp.blocks_per_split - 1) / sp.blocks_per_split;
+  return sp;
+}
+
 // kv_key_bytes: bytes of one key's K and V rows together (sizes the L2 test below)
 void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset, int k_offset, int num_splits,
                  float scale, int dev, long long kv_key_bytes) {
@@ -229,10 +245,9 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
   p.k_offset = k_offset;
   p.num_kblocks = (Nk + kBlockN - 1) / kBlockN;
   p.num_pairs = (Nq + kTilesPerUnit * kBlockM - 1) / (kTilesPerUnit * kBlockM);
-  if (num_splits > p.num_kblocks) num_splits = p.num_kblocks;
-  if (num_splits < 1) num_splits = 1;
-  p.blocks_per_split = (p.num_kblocks + num_splits - 1) / num_splits;
-  p.num_splits = (p.num_kblocks + p.blocks_per_split - 1) / p.blocks_per_split;
+  const SplitPlan sp = split_plan(p.num_kblocks, num_splits);
+  p.blocks_per_split = sp.blocks_per_split;
+  p.num_splits = sp.num_splits;
   p.num_units = BH * p.num_pairs * p.num_splits;
   p.causal = causal ? 1 : 0;
   // zigzag pairing balances causal work but halves the number of items dealt to
@@ -365,7 +380,7 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
   if (!workspace) return ATTN_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
   const HostChunking hcfg = host_chunking(B, H, N, d);
-  if (workspace_bytes < kHostSlots * hcfg.slot_bytes) return ATTN_ERR_DIMS;
+  if (workspace_bytes < kHostSlots * hcfg.slot_bytes) return ATTN_ERR_WORKSPACE;
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
   HostPipe& hp = g_pipe[dev];
@@ -532,7 +547,7 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
   // causal: the queries are the last Nq positions of the Nk keys
   fill_params(p, BH, Nq, Nk, causal, Nk - Nq, 0, num_splits, scale, dev, 4ll * d);
   const long long S = p.num_splits;
-  if (workspace_bytes < splitkv_workspace_bytes(BH, Nq, d, S)) return ATTN_ERR_DIMS;
+  if (workspace_bytes < splitkv_workspace_bytes(BH, Nq, d, S)) return ATTN_ERR_WORKSPACE;
   const long long rows = static_cast<long long>(BH) * Nq;
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = o_part + S * rows * d;
@@ -567,7 +582,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     return ATTN_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_ALIGN;
-  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N)) return ATTN_ERR_DIMS;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N)) return ATTN_ERR_WORKSPACE;
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
   const int BH = B * H;
@@ -612,7 +627,7 @@ const char* attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ATTN_OK";
     case ATTN_ERR_NULL: return "ATTN_ERR_NULL: a required pointer is NULL";
-    case ATTN_ERR_DIMS: return "ATTN_ERR_DIMS: B, H and N must be >= 1";
+    case ATTN_ERR_DIMS: return "ATTN_ERR_DIMS: a size or count is out of range (B, H, N must be >= 1)";
     case ATTN_ERR_UNSUPPORTED_HEADDIM: return "ATTN_ERR_UNSUPPORTED_HEADDIM: d must be 64 or 128";
     case ATTN_ERR_DTYPE: return "ATTN_ERR_DTYPE: unknown dtype";
     case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: tensors must be 16-byte aligned (lse/scales 4-byte)";
@@ -623,6 +638,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_SCALE: return "ATTN_ERR_SCALE: scale must be finite and > 0";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA call failed (no device?)";
     case ATTN_ERR_SCRATCH: return "ATTN_ERR_SCRATCH: the problem needs more than the library's fixed scratch";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: the workspace is smaller than its *_workspace_bytes()";
     default: return "unknown attn_status";
   }
 }
@@ -723,12 +739,9 @@ extern "C" int attn_fwd_splitkv_static(const void* q, const void* k, const void*
     }
   });
   if (sc.status != ATTN_OK) return sc.status;
-  // the number of splits attn_fwd_splitkv will use (it never uses more than the
-  // key blocks allow), and the scratch those need
-  const int nkb = (Nk + kBlockN - 1) / kBlockN;
-  const int s_req = num_splits < nkb ? num_splits : nkb;
-  const int per = (nkb + s_req - 1) / s_req;
-  const int s_eff = (nkb + per - 1) / per;
+  // the number of splits attn_fwd_splitkv will use (the same rule), and the
+  // scratch those need
+  const int s_eff = split_plan((Nk + kBlockN - 1) / kBlockN, num_splits).num_splits;
   if (splitkv_workspace_bytes(static_cast<long long>(B) * H, Nq, d, s_eff) > kStaticScratchBytes)
     return ATTN_ERR_SCRATCH;
   return attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, num_splits, sc.ptr,

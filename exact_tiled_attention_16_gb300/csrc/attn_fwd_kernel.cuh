@@ -96,6 +96,17 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kRegsLaunch * kNumT
 // at most 2^8, which the 16-bit P and the fp32 accumulators absorb.
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kFp8PScaleLog2 = 6.0f;
+// Every kPolyEvery-th pair of scores of a row would take its two exponentials
+// from the FMA pipe (exp2_poly2) instead of the special-function unit; 0 = all
+// on the SFU.  Measured on GB300 (doubled SFU ex2 rate), every share is slower:
+// cfg3-shaped causal d = 128 1659 TFLOP/s at 0, 1621 at 1/8, 1556 at 1/4, 1376
+// at 1/2; d = 64 1022 -> 994 -> 944 -> 741.  The polynomial costs about ten
+// FMA/ALU instructions per pair against two SFU issues, and the softmax is
+// bound by its instruction chain rather than by the SFU's throughput.
+#ifndef ATTN_POLY_EXP2_EVERY
+#define ATTN_POLY_EXP2_EVERY 0
+#endif
+constexpr int kPolyEvery = ATTN_POLY_EXP2_EVERY;
 // Direct-P FP4: TMEM columns (within S_t) of the P scales and the V^T scales
 constexpr uint32_t kFp4SfaCol = 32, kFp4SfbCol = 64;
 
@@ -794,7 +805,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
           for (int c = 0; c < kBlockN; c += 2) {
             const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(cj, cj), make_float2(-m_sub, -m_sub));
-            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            const float2 e = (kPolyEvery > 0 && (c >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1)
+                                 ? exp2_poly2(x)
+                                 : make_float2(ex2_approx(x.x), ex2_approx(x.y));
             acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
             if constexpr (kFp8) pk[c / 2] = pack_f16x2(e.x, e.y);
             else pk[c / 2] = pack_bf16x2(e.x, e.y);

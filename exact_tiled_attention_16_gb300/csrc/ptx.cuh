@@ -320,6 +320,48 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack_f2(a)), "l"(pack_f2(b)));
   return unpack_f2(d);
 }
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack_f2(a)), "l"(pack_f2(b)));
+  return unpack_f2(d);
+}
+// a + b rounded towards -infinity
+__device__ __forceinline__ float2 fadd2_rm(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack_f2(a)), "l"(pack_f2(b)));
+  return unpack_f2(d);
+}
+
+// 2^x for two floats on the FMA pipe, without the special-function unit (which
+// the softmax otherwise saturates with one ex2 per score).
+//   x is clamped to >= -127;  x = n + f with n = floor(x), f in [0, 1);
+//   2^f ~ p(f) = 1 + c1 f + c2 f^2 + c3 f^3;  2^n enters as n added to the
+//   exponent field of p(f).
+// n: adding 1.5 * 2^23 with rounding towards -infinity leaves kMagic + floor(x)
+// exactly (the sum's unit in the last place is 1), with n in the low mantissa
+// bits, so (bits << 23) is n << 23 modulo 2^32.
+// p: c1..c3 minimise the largest relative error of p(f) / 2^f on [0, 1] with the
+// constant term fixed at 1 (Remez exchange; csrc/fit_exp2_poly.py, which prints
+// these float32 values): 8.6e-5 at most in float32 Horner form, below bf16's
+// rounding step (2^-9).  p(0) = 1 exactly makes x <= -127 (and x = -inf, a
+// masked score) give bits 0x3F800000 - (127 << 23) = 0, i.e. +0.0; for x in
+// (-127, -126) the result is a subnormal below 2^-126 (not 2^x, but as
+// negligible).  x is at most a few tens here, far from overflow.
+constexpr float kExp2PolyC1 = 0x1.63e658p-1f;   // 0.695116758
+constexpr float kExp2PolyC2 = 0x1.d2378ap-3f;   // 0.227644995
+constexpr float kExp2PolyC3 = 0x1.3baaa6p-4f;   // 0.0770670399
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  x = make_float2(fmaxf(x.x, -127.f), fmaxf(x.y, -127.f));
+  const float2 j = fadd2_rm(x, make_float2(kMagic, kMagic));         // kMagic + floor(x)
+  const float2 f = fadd2(x, fsub2(make_float2(kMagic, kMagic), j));  // x - floor(x), exact
+  float2 p = ffma2(f, make_float2(kExp2PolyC3, kExp2PolyC3), make_float2(kExp2PolyC2, kExp2PolyC2));
+  p = ffma2(p, f, make_float2(kExp2PolyC1, kExp2PolyC1));
+  p = ffma2(p, f, make_float2(1.f, 1.f));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(j.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(j.y) << 23)));
+}
+
 // Two floats -> packed bf16x2 (round to nearest even); `lo` lands in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

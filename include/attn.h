@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_NULL = -1,                /* a required pointer is NULL */
-  ATTN_ERR_DIMS = -2,                /* B, H or N < 1 */
+  ATTN_ERR_DIMS = -2,                /* a size or count out of range (B, H or N < 1, ...) */
   ATTN_ERR_UNSUPPORTED_HEADDIM = -3, /* d not in {64, 128} */
   ATTN_ERR_DTYPE = -4,               /* dtype not an attn_dtype value */
   ATTN_ERR_ALIGN = -5,               /* q/k/v/o not 16-byte aligned, or lse/scales not 4-byte aligned */
@@ -53,8 +53,23 @@ typedef enum {
   ATTN_ERR_ARCH = -9,                /* the current device is not sm_103 */
   ATTN_ERR_SCALE = -10,              /* scale not finite and > 0 */
   ATTN_ERR_CUDA = -11,               /* a CUDA runtime/driver call failed (e.g. no device) */
-  ATTN_ERR_SCRATCH = -12             /* attn_fwd_splitkv_static: the problem needs more than its fixed scratch */
+  ATTN_ERR_SCRATCH = -12,            /* attn_fwd_splitkv_static: the problem needs more than its fixed scratch */
+  ATTN_ERR_WORKSPACE = -13           /* a caller-supplied workspace is smaller than its *_workspace_bytes() */
 } attn_status;
+/*
+ * Codes 0 .. -9 are the boundary's base set.  The four later codes refine cases
+ * that the base set files under one of its own codes; a caller that only knows
+ * the base set can map them back:
+ *   ATTN_ERR_SCALE     (-10) -> ATTN_ERR_DIMS   an invalid scalar argument
+ *   ATTN_ERR_CUDA      (-11) -> ATTN_ERR_ARCH   no usable sm_103 device (a CUDA
+ *                                              call failed before any launch)
+ *   ATTN_ERR_SCRATCH   (-12) -> ATTN_ERR_OVERFLOW  the problem exceeds a fixed
+ *                                              size limit of the library
+ *   ATTN_ERR_WORKSPACE (-13) -> ATTN_ERR_DIMS   a buffer size argument too small
+ *
+ * `stream` is declared void* so that this header needs no CUDA include: pass a
+ * cudaStream_t (the same pointer); NULL is the legacy default stream.
+ */
 
 typedef enum { ATTN_BF16 = 0 } attn_dtype;
 
@@ -84,9 +99,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *   o          : bf16 [B,H,N,d] output;  lse : float32 [B,H,N] or NULL
  *   d          : 128 (other head dimensions return ATTN_ERR_UNSUPPORTED_HEADDIM)
  *   other arguments as attn_fwd.
- * Arithmetic: e4m3 Q K^T and P V on the tensor cores (fp32 accumulation), softmax
- * in fp32 on the dequantised scores, P rounded to e4m3 (pre-scaled into e4m3's
- * normal range), O rounded to bf16.
+ * Arithmetic: e4m3 Q K^T on the FP8 tensor cores (fp32 accumulation), softmax in
+ * fp32 on the dequantised scores; P rounded to f16 and V's e4m3 codes widened
+ * exactly to f16 on chip, P V on the 16-bit tensor path (an e4m3 P loses too much
+ * once V has outlier channels); O rounded to bf16.
  */
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
                  const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
@@ -131,8 +147,8 @@ int attn_merge(const float* const* o_parts, const float* const* lse_parts, int n
  *            position Nk - Nq + i; requires Nq <= Nk); Nq = Nk is attn_fwd's mask
  *   num_splits : 1..16 (reduced if there are fewer 128-key blocks)
  *   workspace : device scratch of at least attn_splitkv_workspace_bytes(...)
- *               bytes, 16-byte aligned, owned by the caller; its contents on
- *               entry do not matter
+ *               bytes (else ATTN_ERR_WORKSPACE), 16-byte aligned, owned by the
+ *               caller; its contents on entry do not matter
  */
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                      int Nk, int d, int causal, float scale, int num_splits, void* workspace,
@@ -159,7 +175,11 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits)
  * when num_splits * B*H*Nq * (d + 1) * 4 bytes exceed that size (num_splits as
  * reduced to the number of 128-key blocks).  Nothing in this function allocates
  * memory.  The first call on a device looks up the array's device address; make
- * that first call before any stream capture.  All calls share the array (it keeps
+ * that first call before any stream capture.  Under CUDA's default lazy module
+ * loading the library's device code, this array included, is loaded onto a
+ * device by the first library call that needs it there (for any entry point),
+ * which reserves the 32 MiB and may synchronise: make one library call on each
+ * device at start-up, not on a latency-critical path.  All calls share the array (it keeps
  * the last call's contents; every value is rewritten before it is read, so nothing
  * needs clearing): calls whose kernels may overlap on the GPU, such as calls on
  * two streams without ordering between them, race on it and must be avoided.
@@ -177,7 +197,8 @@ size_t attn_splitkv_static_scratch_bytes(void);
  * the device->host copies of a third run on separate streams, so the transfers
  * overlap the computation.  Outputs are bitwise those of attn_fwd.
  *   workspace : device scratch of at least attn_fwd_host_workspace_bytes(B,H,N,d)
- *               bytes, 256-byte aligned, owned by the caller; the call overwrites it
+ *               bytes (else ATTN_ERR_WORKSPACE), 256-byte aligned, owned by the
+ *               caller; the call overwrites it
  *   stream    : the kernels run on it; work queued on it after this call sees
  *               the outputs in host memory.  Calls that share a workspace must
  *               be queued on the same stream.
@@ -221,8 +242,8 @@ int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* 
  *   lse              : const float32 [B,H,N]
  *   dq, dk, dv       : bf16 [B,H,N,d] outputs, 16-byte aligned
  *   workspace        : device scratch of at least attn_bwd_workspace_bytes(B,H,N)
- *                      bytes (16-byte aligned), owned by the caller; the call
- *                      overwrites it
+ *                      bytes (else ATTN_ERR_WORKSPACE; 16-byte aligned), owned by
+ *                      the caller; the call overwrites it
  *   d : 64 or 128; other arguments as attn_fwd.  Deterministic (no atomics).
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -256,6 +277,30 @@ int attn_set_wait_timeout_ns(unsigned long long ns);
  * attn_check_device_errors returns (ATTN_ERR_TIMEOUT when the wait is working).
  */
 int attn_selftest_wait_timeout(void* stream);
+
+/*
+ * attn_measure_exp2_rates -- diagnostics (no counterpart on the pages): the
+ * throughput of the two exponentials the forward kernel's softmax uses, in
+ * exponentials per SM clock cycle per SM, measured on the current device:
+ *   *sfu_per_clk_sm      : ex2.approx on the special-function unit
+ *   *fma_poly_per_clk_sm : the FMA-pipe polynomial exponential (two per call)
+ * Each is one launch of #SM CTAs of 512 threads running eight independent chains
+ * x = 2^-x, timed with the SM cycle counter (longest CTA).  Host output pointers;
+ * the call synchronises `stream`.  Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_ARCH,
+ * ATTN_ERR_LAUNCH or ATTN_ERR_CUDA.
+ */
+int attn_measure_exp2_rates(float* sfu_per_clk_sm, float* fma_poly_per_clk_sm, void* stream);
+
+/*
+ * attn_eval_exp2 -- diagnostics (no counterpart on the pages): evaluates both
+ * exponentials on n device floats x: y_poly = the FMA-pipe polynomial (x clamped
+ * to >= -127, 2^floor(x) times a degree-3 fit of 2^f with p(0) = 1, relative
+ * error <= 8.6e-5 above 2^-126, +0.0 for x <= -127), y_sfu = ex2.approx.ftz.
+ * x, y_poly, y_sfu: device float arrays of n >= 1 elements, 4-byte aligned.
+ * Asynchronous on `stream`.  Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_DIMS,
+ * ATTN_ERR_ALIGN, ATTN_ERR_ARCH, ATTN_ERR_LAUNCH or ATTN_ERR_CUDA.
+ */
+int attn_eval_exp2(const float* x, float* y_poly, float* y_sfu, long long n, void* stream);
 
 #ifdef __cplusplus
 }

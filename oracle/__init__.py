@@ -6,4 +6,4 @@ this package.  The library's compute path never calls it.
 from .attention import attention_head, attention, attention_probs  # noqa: F401
 from .attention_bwd import (attention_bwd_head, attention_bwd, attention_bwd_query_rows,  # noqa: F401
                             attention_bwd_key_rows)
-from .direct_p import direct_p_head, direct_p_attention, direct_p_probs  # noqa: F401
+from .direct_p import direct_p_head, direct_p_probs  # noqa: F401

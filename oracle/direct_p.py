@@ -94,14 +94,3 @@ def direct_p_head(q, k, v, causal, scale, rows=None):
     o = (p @ v) / l[:, None]
     return o, np.log(l)
 
-
-def direct_p_attention(q, k, v, causal, scale):
-    """[B, H, N, d] arrays -> (o, lse) float64."""
-    q = np.asarray(q)
-    B, H = q.shape[:2]
-    o = np.empty(q.shape[:3] + (np.asarray(v).shape[-1],))
-    lse = np.empty(q.shape[:3])
-    for b in range(B):
-        for h in range(H):
-            o[b, h], lse[b, h] = direct_p_head(q[b, h], k[b, h], v[b, h], causal, scale)
-    return o, lse

@@ -37,10 +37,11 @@ def row_allowances(q, k, v, causal, scale, rows):
     t = (scale * dp.LOG2E) * (q[rows] @ k.T)
     if causal:
         t = np.where(np.arange(k.shape[0])[None, :] > rows[:, None], -np.inf, t)
+    # the compared values come from the oracle itself; p and E (its steps 2-3)
+    # only size the allowances below
+    o, lse = dp.direct_p_head(q, k, v, causal, scale, rows=rows)
     p, _, E = dp.direct_p_probs(t)
-    l = p.sum(axis=1)
-    o = (p @ v) / l[:, None]
-    lse = np.log(l)
+    l = np.exp(lse)
     R, N = t.shape
     finite = np.isfinite(t)
     tmax = np.where(finite, np.abs(t), 0).max(axis=1, keepdims=True)

@@ -57,22 +57,41 @@ def run_fp8(w: synth.Workload, dev="cuda", want_lse=True):
     return o_np, lse_np
 
 
-def assert_fp8_tol(stats, what=""):
+def assert_fp8_tol(stats, what="", detail=None):
+    """The FP8 bound (the 6e-2 budget beyond the bf16 output's own rounding).
+    With `detail` from compare_rows it also holds the literal max|dO| <= 6e-2 on
+    the elements where bf16 can represent it (|O_ref| < 16) and prints the raw
+    maxima, so that the margin of the reading is visible in the test log."""
     max_o, mean_o, max_l, max_excess = stats
     assert max_excess <= FP8_MAX_ABS_O, \
         f"{what} max(|dO| - 2^-8 |O|) {max_excess:.4g} > {FP8_MAX_ABS_O} (max|dO| {max_o:.4g})"
     assert max_l <= BF16_MAX_ABS_LSE, f"{what} max|dLSE| {max_l:.4g} > {BF16_MAX_ABS_LSE}"
+    if detail is not None:
+        print(f"[fp8 raw] {what}: max|dO| {detail['max_abs_o']:.4g}, vs bf16-rounded oracle "
+              f"{detail['max_abs_o_vs_bf16_ref']:.4g}, where |O|<16 {detail['max_abs_o_small']:.4g}, "
+              f"beyond output rounding {detail['max_excess']:.4g}")
+        assert detail["max_abs_o_small"] <= FP8_MAX_ABS_O, \
+            f"{what} max|dO| over |O_ref| < 16 {detail['max_abs_o_small']:.4g} > {FP8_MAX_ABS_O}"
 
 
-def compare_rows(w: synth.Workload, o_np, lse_np, rows_per_head=None, seed_rows=0, excess=False):
+def compare_rows(w: synth.Workload, o_np, lse_np, rows_per_head=None, seed_rows=0, excess=False, detail=None):
     """Compares the GPU result with the oracle on all rows (rows_per_head None)
     or on a seeded sample of rows per head.  Returns (max|dO|, mean|dO|,
-    max|dLSE|) and, with excess=True, also max(|dO| - 2^-8 |O_ref|)."""
+    max|dLSE|) and, with excess=True, also max(|dO| - 2^-8 |O_ref|).
+
+    If a dict is given as `detail`, it receives the raw figures behind the FP8
+    bound: "max_abs_o" (max|dO| against the fp64 oracle), "max_abs_o_vs_bf16_ref"
+    (against the oracle's O rounded to bf16, which removes the output's own
+    rounding up to one bf16 step where the two roundings fall apart) and
+    "max_abs_o_small" (max|dO| over the elements with |O_ref| < 16, where bf16's
+    half-step 2^-5 still fits inside 6e-2, so the literal bound applies)."""
     max_x = -np.inf
     max_o = 0.0
     sum_o = 0.0
     cnt = 0
     max_l = 0.0
+    max_r = 0.0
+    max_s = 0.0
     for b in range(w.B):
         for h in range(w.H):
             q, k, v = w.head_f64(b, h)
@@ -81,12 +100,20 @@ def compare_rows(w: synth.Workload, o_np, lse_np, rows_per_head=None, seed_rows=
             go = o_np[b, h] if rows is None else o_np[b, h][rows]
             d = np.abs(go - ro)
             max_o = max(max_o, float(d.max()))
+            if detail is not None:
+                ro_bf16 = synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(ro.astype(np.float32)))
+                max_r = max(max_r, float(np.abs(go - ro_bf16).max()))
+                small = np.abs(ro) < 16.0
+                if small.any():
+                    max_s = max(max_s, float(d[small].max()))
             max_x = max(max_x, float((d - BF16_UNIT_ROUNDOFF * np.abs(ro)).max()))
             sum_o += float(d.sum())
             cnt += d.size
             if lse_np is not None:
                 gl = lse_np[b, h] if rows is None else lse_np[b, h][rows]
                 max_l = max(max_l, float(np.abs(gl - rl).max()))
+    if detail is not None:
+        detail.update(max_abs_o=max_o, max_abs_o_vs_bf16_ref=max_r, max_abs_o_small=max_s, max_excess=max_x)
     if excess:
         return max_o, sum_o / cnt, max_l, max_x
     return max_o, sum_o / cnt, max_l

@@ -47,7 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     import exact_tiled_attention_16_gb300._lib as L
     assert L.attn_status_string(0) == "ATTN_OK"
-    for code in range(-11, 0):
+    for code in range(-13, 0):
         assert L.attn_status_string(code).startswith("ATTN_ERR_")
     assert "unknown" in L.attn_status_string(-999)
 
@@ -121,7 +121,7 @@ def test_fwd_host_validation(lib):
         return L.attn_fwd_host_raw(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 2, 3, 100, d, 0, 0.125, ws, nbytes, 0)
     assert call(ws=0) == -1
     assert call(ws=0x10010) == -5
-    assert call(nbytes=need - 1) == -2
+    assert call(nbytes=need - 1) == -13
     assert call(d=96) == -3
 
 
@@ -172,7 +172,7 @@ def test_bwd_validation(lib):
     assert call(lse=0x6002) == -5
     assert call(workspace=0xa008) == -5
     # two float arrays of B*H rows of N rounded up to 128
-    assert call(workspace_bytes=2047) == -2
+    assert call(workspace_bytes=2047) == -13
     assert L.bwd_workspace_bytes(1, 2, 100) == 2 * 2 * 128 * 4
     assert L.bwd_workspace_bytes(2, 3, 257) == 2 * 6 * 384 * 4
     assert L.bwd_workspace_bytes(0, 2, 100) == 0

@@ -198,6 +198,6 @@ def test_workspace_too_small_launches_nothing():
     p = q.data_ptr()
     rc = L.attn_bwd_raw(p, p, p, p, p, lse.data_ptr(), dq.data_ptr(), dq.data_ptr(), dq.data_ptr(), 1, 1, 128, 64,
                         False, 0.125, ws.data_ptr(), 127 * 4, torch.cuda.current_stream().cuda_stream)
-    assert rc == -2
+    assert rc == L.ATTN_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert (dq.float() == 7.0).all()

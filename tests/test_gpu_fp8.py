@@ -30,7 +30,8 @@ def test_fp8_small_full_oracle(shape, causal):
     B, H, N = shape
     w = synth.make_fp8(B, H, N, 128, causal, seed=200 + N)
     o, lse = run_fp8(w)
-    assert_fp8_tol(compare_rows(w, o, lse, excess=True), f"fp8 {shape} causal={causal}")
+    det = {}
+    assert_fp8_tol(compare_rows(w, o, lse, excess=True, detail=det), f"fp8 {shape} causal={causal}", det)
 
 
 @pytest.mark.parametrize("shape", [(2, 40, 1024), (1, 76, 2304)], ids=["pairs4_2rounds", "pairs9_odd_5rounds"])
@@ -42,20 +43,23 @@ def test_fp8_causal_many_units(shape):
     w = synth.make_fp8(B, H, N, 128, True, seed=500 + N)
     o, lse = run_fp8(w)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
-    assert_fp8_tol(compare_rows(w, o, lse, rows_per_head=64, excess=True), f"fp8 causal {shape}")
+    det = {}
+    assert_fp8_tol(compare_rows(w, o, lse, rows_per_head=64, excess=True, detail=det), f"fp8 causal {shape}", det)
 
 
 def test_fp8_no_outliers_no_rotation():
     w = synth.make_fp8(1, 2, 640, 128, False, seed=7, outlier_frac=0.0, rotate=False)
     o, lse = run_fp8(w)
-    assert_fp8_tol(compare_rows(w, o, lse, excess=True), "plain fp8")
+    det = {}
+    assert_fp8_tol(compare_rows(w, o, lse, excess=True, detail=det), "plain fp8", det)
 
 
 def test_cfg5_sampled_rows():
     w = synth.make_config("cfg5")
     o, lse = run_fp8(w)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
-    assert_fp8_tol(compare_rows(w, o, lse, rows_per_head=256, excess=True), "cfg5")
+    det = {}
+    assert_fp8_tol(compare_rows(w, o, lse, rows_per_head=256, excess=True, detail=det), "cfg5", det)
 
 
 def test_fp8_error_is_mostly_output_rounding():

@@ -74,6 +74,6 @@ def test_workspace_too_small_launches_nothing():
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     rc = L.attn_fwd_host_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), 0, 1, 2, 256, 64, 0, 0.125,
                              ws.data_ptr(), need - 256, torch.cuda.current_stream().cuda_stream)
-    assert rc == -2
+    assert rc == L.ATTN_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert (o.float() == 7.0).all()

@@ -191,4 +191,4 @@ def test_splitkv_deterministic_and_workspace_checked():
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     rc = L.attn_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o1.data_ptr(), 0, 1, 2, 1024, 1024, 64,
                                 False, 0.125, 4, small.data_ptr(), 16, torch.cuda.current_stream().cuda_stream)
-    assert rc == -2
+    assert rc == L.ATTN_ERR_WORKSPACE

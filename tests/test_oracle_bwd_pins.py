@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from oracle.attention import attention_head
-from oracle.attention_bwd import attention_bwd_head, attention_bwd_key_rows, attention_bwd_query_rows
+from oracle.attention_bwd import attention_bwd, attention_bwd_head, attention_bwd_key_rows, attention_bwd_query_rows
 
 
 def _loss(q, k, v, do, causal, scale):
@@ -130,3 +130,47 @@ def test_bwd_planted_mistake_is_caught(kind):
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+def _batched_autograd(q, k, v, do, causal, scale):
+    torch = pytest.importorskip("torch")
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+    o.backward(torch.tensor(do))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def _batched_swapped(q, k, v, do, causal, scale):
+    """A planted (b, h) indexing slip: head (b, h) written to slot (h, b) of a
+    transposed batch layout, then transposed back the wrong way."""
+    B, H = q.shape[:2]
+    out = [np.empty(x.shape, np.float64) for x in (q, k, v)]
+    for b in range(B):
+        for h in range(H):
+            g = attention_bwd_head(q[b, h], k[b, h], v[b, h], do[b, h], causal, scale)
+            bb, hh = divmod(h * B + b, H)
+            for o_, x in zip(out, g):
+                o_[bb, hh] = x
+    return tuple(out)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batched_bwd_matches_autograd_and_heads(causal):
+    """The batched gradient oracle (the smoke check's reference) against torch
+    autograd through float64 scaled_dot_product_attention on a [B, H, N, d]
+    batch of distinct heads, and head by head against attention_bwd_head; a
+    (b, h) indexing slip fails it (B != H, so any mix-up of heads shows)."""
+    g = np.random.default_rng(9)
+    B, H, N, d = 2, 3, 17, 8
+    q, k, v, do = (g.standard_normal((B, H, N, d)) for _ in range(4))
+    scale = 0.35
+    got = attention_bwd(q, k, v, do, causal, scale)
+    ref = _batched_autograd(q, k, v, do, causal, scale)
+    for a, b in zip(got, ref):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
+    for b in range(B):
+        for h in range(H):
+            for a, r in zip(got, attention_bwd_head(q[b, h], k[b, h], v[b, h], do[b, h], causal, scale)):
+                np.testing.assert_array_equal(a[b, h], r)
+    bad = _batched_swapped(q, k, v, do, causal, scale)
+    assert any(not np.allclose(a, r, rtol=1e-6, atol=1e-8) for a, r in zip(bad, ref))
