@@ -48,10 +48,14 @@ METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense BF16/FP8 tensor peak"
 METRIC_BWD = "attention bwd TFLOP/s on 1 GB300 (counted as 2.5x forward flops) and % of dense BF16 tensor peak"
 BWD_FLOP_RATIO = 2.5
 L2_BYTES = 126 * 1024 * 1024
-KERNEL_SOURCES = ["exact_tiled_attention_16_gb300/csrc/attn_fwd_kernel.cuh",
-                  "exact_tiled_attention_16_gb300/csrc/attn_bwd_kernel.cuh",
-                  "exact_tiled_attention_16_gb300/csrc/ptx.cuh",
-                  "exact_tiled_attention_16_gb300/csrc/attn_api.cu"]
+CSRC = os.path.join(ROOT, "exact_tiled_attention_16_gb300", "csrc")
+# tensor-core work per SM clock: a 128 x 128 x 16 kind::f16 MMA occupies the pipe
+# 64 cycles (measured), 8192 flops per cycle; the e4m3 Q K^T at the nominal 2x
+ALL_WORKLOADS = ["cfg1", "cfg2n", "cfg2c", "cfg3", "cfg4", "cfg5", "cfg5p", "decode",
+                 "custom:1,32,4096,128,0", "custom:1,32,8192,128,0", "custom:1,32,16384,128,0",
+                 "bwd:cfg3", "bwd:cfg4"]
+BF16_FLOP_PER_CLK_SM = 8192.0
+FP8_FLOP_PER_CLK_SM = 16384.0
 WORKLOAD_TEXT = {
     "cfg1": "bf16 B1 H2 N128 d64 non-causal",
     "cfg2n": "bf16 B4 H16 N2048 d128 non-causal",
@@ -65,12 +69,32 @@ WORKLOAD_TEXT = {
 DECODE = dict(B=2, H=16, Nq=512, Nk=65536, d=128, seed=6)
 
 
+def kernel_sources():
+    return sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".inc")))
+
+
 def kernel_hash() -> str:
+    """Hash of every CUDA source of the library (what a profile was taken on)."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
+    for f in kernel_sources():
+        with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def kernel_instance(dtype: str, d: int, partial: bool = False) -> str:
+    """The forward kernel's template instance as ncu names it, read from the
+    instance table of attn_api.cu (D, K stages, V stages, fp8, partial, fp4)."""
+    import re
+    text = open(os.path.join(CSRC, "attn_api.cu")).read()
+    inst = dict(re.findall(r"#define (ATTN_\w+_D\d+) (\d+, \d+, \d+, (?:true|false))", text))
+    key = {"bf16": f"ATTN_BF16_D{d}", "e4m3": f"ATTN_FP8_D{d}", "e4m3_e2m1": f"ATTN_FP4_D{d}"}[dtype]
+    if key not in inst:
+        return "attn::attn_fwd_kernel<?>"
+    D, nk, nv, fp8 = (x.strip() for x in inst[key].split(","))
+    fp4 = dtype == "e4m3_e2m1"
+    args = [D, nk, nv, "1" if fp8 == "true" else "0", "1" if partial else "0", "1" if fp4 else "0"]
+    return "attn::attn_fwd_kernel<" + ", ".join(args) + ">"
 
 
 def measured_peaks():
@@ -177,6 +201,64 @@ def make_decode_workload():
     return w
 
 
+def _blas_threads() -> int:
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", str(_CORES)))
+
+
+def make_workload(args):
+    """The synthetic workload the flags name (seeded; see synth.py)."""
+    if args.custom:
+        B, H, N, d, c = (int(x) for x in args.custom.split(","))
+        return synth.make_bf16(B, H, N, d, bool(c), seed=3, name=f"custom_B{B}H{H}N{N}d{d}{'c' if c else 'n'}")
+    if args.workload == "decode":
+        return make_decode_workload()
+    return synth.make_config(args.workload)
+
+
+def cpu_row_probe(args):
+    """(run in a child process with the BLAS thread count pinned by its
+    environment) times the oracle on sampled rows and prints one JSON object."""
+    w = make_workload(args)
+    fn = cpu_oracle_bwd_rate if args.bwd_pass == "bwd" else cpu_oracle_rate
+    val, desc, secs, rows = fn(w, args.cpu_budget, rows_per_head=args.probe_rows)
+    print(json.dumps({"value": val, "ms_per_row": secs * 1e3 / max(rows, 1), "rows": rows, "seconds": secs,
+                      "threads": _blas_threads(), "sample": desc}), flush=True)
+
+
+def cpu_rows_one_thread(args):
+    """ms per query row of the oracle with one BLAS thread (child process)."""
+    env = dict(os.environ)
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-row-probe", "--cpu-budget", str(args.cpu_budget / 3),
+           "--probe-rows", "32", "--pass", args.bwd_pass]
+    cmd += ["--custom", args.custom] if args.custom else ["--workload", args.workload]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError):
+        return None
+
+
+def run_all(args):
+    """One JSON line per workload of ALL_WORKLOADS (each its own child process)."""
+    for spec in ALL_WORKLOADS:
+        cmd = [sys.executable, os.path.abspath(__file__), "--steps", str(args.steps), "--warmup", str(args.warmup),
+               "--cpu-budget", str(args.cpu_budget)]
+        if spec.startswith("custom:"):
+            cmd += ["--custom", spec.split(":", 1)[1]]
+        elif spec.startswith("bwd:"):
+            cmd += ["--workload", spec.split(":", 1)[1], "--pass", "bwd"]
+        else:
+            cmd += ["--workload", spec]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+        if r.returncode != 0 or not lines:
+            print(json.dumps({"workload": spec, "error": (r.stderr or r.stdout)[-400:]}), flush=True)
+            continue
+        print(lines[-1], flush=True)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -212,8 +294,8 @@ def cpu_oracle_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 256
             break
     what = "Direct-P oracle: " if w.dtype == "e4m3_e2m1" else ""
     desc = (f"{what}{rows_done} query rows ({rows_per_head} seeded rows per head x {heads} heads) against all "
-            f"visible keys of {w.name}; fp64 numpy, {_CORES} BLAS threads")
-    return flops / elapsed / 1e12, desc, elapsed
+            f"visible keys of {w.name}; fp64 numpy, {_blas_threads()} BLAS threads")
+    return flops / elapsed / 1e12, desc, elapsed, rows_done
 
 
 def cpu_oracle_bwd_rate(w: synth.Workload, budget_s: float, rows_per_head: int = 128, max_heads=None):
@@ -243,8 +325,8 @@ def cpu_oracle_bwd_rate(w: synth.Workload, budget_s: float, rows_per_head: int =
         if done:
             break
     desc = (f"dq of {rows_done} query rows ({rows_per_head} seeded rows per head x {heads} heads) of "
-            f"{w.name}, each counted as 2.5x its forward flops; fp64 numpy, {_CORES} BLAS threads")
-    return flops / elapsed / 1e12, desc, elapsed
+            f"{w.name}, each counted as 2.5x its forward flops; fp64 numpy, {_blas_threads()} BLAS threads")
+    return flops / elapsed / 1e12, desc, elapsed, rows_done
 
 
 def run_reference(args, world, rank):
@@ -297,7 +379,8 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_block(args, w),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle", "sample": sample,
+                         "ms_per_row_all_cores": tot_t * 1e3 / (args.steps * rows_per_step), "nproc": os.cpu_count()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -333,9 +416,20 @@ def main():
     ap.add_argument("--custom", default=None,
                     help="B,H,N,d,causal: a seeded bf16 workload of that shape instead of --workload "
                          "(for profiling captures on a reduced case)")
+    ap.add_argument("--all", action="store_true",
+                    help="one JSON line for each workload (BASELINE configs, Direct-P, decode, the non-causal "
+                         "d=128 points N=4096/8192/16384, the backward of cfg3 and cfg4)")
+    ap.add_argument("--cpu-row-probe", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--probe-rows", type=int, default=256, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.cpu_row_probe:
+        cpu_row_probe(args)
+        return
+    if args.all:
+        run_all(args)
+        return
 
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -354,13 +448,7 @@ def main():
         pg = dist
 
     decode = args.workload == "decode" and not args.custom
-    if args.custom:
-        B, H, N, d, c = (int(x) for x in args.custom.split(","))
-        w = synth.make_bf16(B, H, N, d, bool(c), seed=3, name=f"custom_B{B}H{H}N{N}d{d}{'c' if c else 'n'}")
-    elif decode:
-        w = make_decode_workload()
-    else:
-        w = synth.make_config(args.workload)
+    w = make_workload(args)
     fp4 = w.dtype == "e4m3_e2m1"
     fp8 = w.dtype == "e4m3" or fp4
     bwd = args.bwd_pass == "bwd"
@@ -517,13 +605,48 @@ def main():
     peak = float(peaks["bf16_tflops"]) * ratio
     src = (f"{peak_src} bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json)" if peak_src == "measured"
            else "fallback 1.9 PFLOP/s bf16") + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else "")
-    kname = "attn_bwd: prep + dq + dkdv kernels (whole step)" if bwd else {("e4m3_e2m1", 128): "attn_fwd_kernel<128,4,4,fp8,final,fp4>",
-                                                                         ("bf16", 64): "attn_fwd_kernel<64,4,4,false>", ("bf16", 128): "attn_fwd_kernel<128,2,2,false>",
-             ("e4m3", 128): "attn_fwd_kernel<128,3,3,true>"}.get((w.dtype, w.d), "attn_fwd_kernel")
+    if bwd:
+        kname = (f"attn::attn_bwd_prep_kernel<{w.d}> + attn::attn_bwd_dq_kernel + attn::attn_bwd_dkdv_kernel "
+                 "(whole step)")
+    elif decode:
+        kname = kernel_instance(w.dtype, w.d, partial=True) + " + attn::attn_merge_kernel"
+    else:
+        kname = kernel_instance(w.dtype, w.d)
+    clocks = clk.summary()
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic_for(w.name + (":bwd" if bwd else "")), "peak_source": src,
             "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * ratio),
-            "kernel": kname, "avg_launch_ms": avg_kernel_ms, "flops_per_launch": flops}
+            "kernel": kname, "kernel_hash": kernel_hash(), "avg_launch_ms": avg_kernel_ms, "flops_per_launch": flops}
+    # Two more ceilings at the clock the SMs ran at during the timed region:
+    #  * the tensor pipe's own rate (the measured 128x128x16 MMA time; e4m3 Q K^T
+    #    at the nominal 2x), which cuBLAS's measured peak stays below;
+    #  * the special-function unit: one ex2 per score (two in the backward, whose
+    #    passes both recompute P) against 4 d counted flops per score (10 d in the
+    #    backward), at the ex2 rate measured on this GPU now.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    hz = mhz * 1e6
+    if fp4:
+        pipe_fpc = 1.0 / (0.5 / FP8_FLOP_PER_CLK_SM + 0.5 / (3.0 * FP8_FLOP_PER_CLK_SM))
+    elif fp8:
+        pipe_fpc = 1.0 / (0.5 / FP8_FLOP_PER_CLK_SM + 0.5 / BF16_FLOP_PER_CLK_SM)
+    else:
+        pipe_fpc = BF16_FLOP_PER_CLK_SM
+    roof["pipe_peak"] = pipe_fpc * sms * hz / 1e12
+    roof["frac_of_pipe_peak"] = achieved / roof["pipe_peak"]
+    roof["pipe_peak_source"] = (f"{pipe_fpc:.0f} flop/clk/SM x {sms} SMs x {mhz:.0f} MHz (median SM clock of the "
+                                "timed region); 8192 = a 128x128x16 bf16 MMA per 64 cycles, measured"
+                                + ("; e4m3 Q K^T at the nominal 2x" if fp8 else ""))
+    try:
+        sfu_rate, poly_rate = pkg.measure_exp2_rates()
+        exps, fl = (2.0, 10.0 * w.d) if bwd else (1.0, 4.0 * w.d)
+        roof["sfu_ceiling"] = fl / exps * sfu_rate * sms * hz / 1e12
+        roof["sfu_ceiling_source"] = (f"ex2.approx measured {sfu_rate:.2f}/clk/SM (FMA-pipe polynomial "
+                                      f"{poly_rate:.2f}); {exps:.0f} exponential(s) per score against "
+                                      f"{fl:.0f} counted flops per score")
+    except Exception as e:  # the ceiling is context; its absence must not void the line
+        roof["sfu_ceiling"] = None
+        roof["sfu_ceiling_source"] = f"not measured: {e}"
     if fp4:
         # Q K^T on the fp8 path (2x bf16), P V on the FP4 path (6x bf16: nominal
         # 13.5 / 2.25 PFLOP/s): the roof of that mix is 1 / (0.5/fp8 + 0.5/fp4)
@@ -553,12 +676,17 @@ def main():
                 "api": ("attn_fwd_host: pinned host buffers, chunked copies overlapped with the kernels"
                         if host_api else "pinned host copies in, the pass, copies out, on one stream")},
         "gpu_launches": args.steps * launches_per_step,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        val, desc, secs = (cpu_oracle_bwd_rate if bwd else cpu_oracle_rate)(w, args.cpu_budget)
+        val, desc, secs, rows = (cpu_oracle_bwd_rate if bwd else cpu_oracle_rate)(w, args.cpu_budget)
+        one = cpu_rows_one_thread(args)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
-                                "sample": desc, "seconds": secs}
+                                "sample": desc, "seconds": secs,
+                                "ms_per_row_all_cores": secs * 1e3 / max(rows, 1),
+                                "ms_per_row_1_thread": one["ms_per_row"] if one else None,
+                                "sample_1_thread": one["sample"] if one else "not measured",
+                                "nproc": os.cpu_count()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:

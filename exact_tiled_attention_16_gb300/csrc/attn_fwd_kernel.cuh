@@ -107,6 +107,8 @@ constexpr float kFp8PScaleLog2 = 6.0f;
 #define ATTN_POLY_EXP2_EVERY 0
 #endif
 constexpr int kPolyEvery = ATTN_POLY_EXP2_EVERY;
+
+
 // Direct-P FP4: TMEM columns (within S_t) of the P scales and the V^T scales
 constexpr uint32_t kFp4SfaCol = 32, kFp4SfbCol = 64;
 
@@ -149,7 +151,7 @@ struct TileLayout {
 
 // Shared-memory plan of one instance: Q tiles, K ring, V ring and (FP8) the f16
 // copy of V, then the mbarriers.
-template <int D, int NK, int NV, bool kFp8, bool kFp4 = false>
+template <int D, int NK, int NV, bool kFp8, bool kFp4 = false, bool kTmaO = false>
 struct SmemPlan {
   using In = TileLayout<D, kFp8 ? 1 : 2>;   // Q, K, V as loaded
   using V16 = TileLayout<D, 2>;              // V operand of P V (bf16 or f16)
@@ -160,8 +162,12 @@ struct SmemPlan {
   static constexpr uint32_t kK = kQ + kTilesPerUnit * In::kTileBytes;
   static constexpr uint32_t kV = kK + NK * In::kTileBytes;
   static constexpr uint32_t kC = kV + NV * kVTileBytes;
-  static constexpr uint32_t kBars = kC + kNumConv * V16::kTileBytes;
-  static constexpr int kNumBars = 14 + 2 * NK + 2 * NV + 2 * kNumConv;
+  // TMA store of O (kTmaO): per tile a 128 x 64 bf16 staging chunk (128-byte
+  // swizzle)
+  static constexpr uint32_t kOst = kC + kNumConv * V16::kTileBytes;
+  static constexpr uint32_t kOstChunkBytes = kBlockM * 128;
+  static constexpr uint32_t kBars = kOst + (kTmaO ? kTilesPerUnit * kOstChunkBytes : 0);
+  static constexpr int kNumBars = 18 + 2 * NK + 2 * NV + 2 * kNumConv;
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBars + 8 * kNumBars + 16;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
@@ -252,6 +258,19 @@ __device__ __forceinline__ int unit_for_round(int round, const FwdParams& p) {
   return pos < p.num_units ? pos : kNoMoreUnits;
 }
 
+// Largest of 128 scores: four independent chains of three-input max.
+__device__ __forceinline__ float row_max128(const float (&s)[kBlockN]) {
+  float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]), a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
+#pragma unroll
+  for (int c = 8; c < kBlockN; c += 8) {
+    a0 = fmax3(a0, s[c], s[c + 1]);
+    a1 = fmax3(a1, s[c + 2], s[c + 3]);
+    a2 = fmax3(a2, s[c + 4], s[c + 5]);
+    a3 = fmax3(a3, s[c + 6], s[c + 7]);
+  }
+  return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+}
+
 // A wait taken by all 32 lanes of a warp that returns the same answer on every
 // lane, so that the warp stays converged for the .sync.aligned tcgen05 ops.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -271,13 +290,17 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 
 // kPartial selects the output: false = normalised bf16 O and lse (every query
 // row sees key 0: no position offsets, no splits); true = per-split fp32 O and
-// lse, where a tile or row may see no key at all.
-template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false>
+// lse, where a tile or row may see no key at all.  kTmaO (final bf16 output
+// only): O leaves through shared-memory staging and TMA stores instead of
+// row-per-thread global stores.
+template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+                const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                const FwdParams p) {
   static_assert(!kFp4 || (kFp8 && D == 128 && !kPartial), "Direct-P FP4: e4m3 Q K^T, d = 128, final output");
-  using Plan = SmemPlan<D, NK, NV, kFp8, kFp4>;
+  static_assert(!kTmaO || !kPartial, "the TMA store serves the final bf16 output");
+  using Plan = SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO>;
   using L = typename Plan::In;
   using LV = typename Plan::V16;
   constexpr uint32_t kTmemS[2] = {0, 128};
@@ -293,6 +316,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const uint32_t sK = base + Plan::kK;
   const uint32_t sV = base + Plan::kV;
   const uint32_t sC = base + Plan::kC;  // FP8: f16 V buffers
+  const uint32_t sOst = base + Plan::kOst;  // + t * kOstChunkBytes: O staging of tile t
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Plan::kBars);
   const uint32_t b_q_full = smem_u32(&bars[0]);
   const uint32_t b_q_empty = smem_u32(&bars[1]);
@@ -308,6 +332,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const uint32_t b_c_full = smem_u32(&bars[12 + 2 * NK + 2 * NV]);  // + 8 b (FP8)
   const uint32_t b_c_empty = b_c_full + 8 * Plan::kNumConv;
   const uint32_t b_pa_full = b_c_empty + 8 * Plan::kNumConv;  // + 8 t: first half of P_t written
+  const uint32_t b_ost_ready = b_pa_full + 8 * kTilesPerUnit;   // + 8 t: staging chunk of tile t written
+  const uint32_t b_ost_free = b_ost_ready + 8 * kTilesPerUnit;  // + 8 t: ... read by its TMA store
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[Plan::kNumBars]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -325,6 +351,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       mbar_init(b_pv_done + 8 * t, 1);
       mbar_init(b_o_free + 8 * t, 128);
       mbar_init(b_pa_full + 8 * t, 128);
+      mbar_init(b_ost_ready + 8 * t, 128);
+      mbar_init(b_ost_free + 8 * t, 1);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(b_k_full + 8 * s, 1);
@@ -345,6 +373,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
+    if constexpr (kTmaO) prefetch_tmap(&tmap_o);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -536,12 +565,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             tc_fence_after();
             if constexpr (kFp4) issue_pv(t, v_base, j > 0, -1);
             else issue_pv(t, v_base, true, 1);
+            // tile 1 is the last user of V_j and K_{j+1}.  BF16: V_j's stage is
+            // released as soon as P_1 V_j completes, ahead of the next Q K^T, so
+            // that V_{j+2} starts loading earlier (d = 128 +1.8%); FP8 releases
+            // its f16 copy after the Q K^T (earlier was 2% slower).
+            constexpr bool kEarlyV = !kFp8;
+            if (kEarlyV && t == 1) mma_commit(b_v_empty + 8 * (gj % NV));
             if (j + 1 < nt) issue_s(t, skn);
             if (j == nt - 1) mma_commit(b_pv_done + 8 * t);
             if (t == 1) {
-              // tile 1 is the last user of V_j and K_{j+1}
-              if constexpr (Plan::kNumConv > 0) mma_commit(b_c_empty + 8 * (gj & 1));
-              else mma_commit(b_v_empty + 8 * (gj % NV));
+              if constexpr (!kEarlyV) {
+                if constexpr (Plan::kNumConv > 0) mma_commit(b_c_empty + 8 * (gj & 1));
+                else mma_commit(b_v_empty + 8 * (gj % NV));
+              }
               if (j + 1 < nt) {
                 mma_commit(b_k_empty + 8 * skn);
                 if (j + 1 == n1 - 1) mma_commit(b_q_empty);
@@ -611,6 +647,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const uint32_t tS = tmem + lane_addr + kTmemS[t];
     const uint32_t tO = tmem + lane_addr + kTmemO[t];
     uint32_t s_iter = 0, pv_iter = 0;
+    uint32_t ost_uses = 0;  // TMA stores of O issued from this tile's staging chunk
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int u = unit_for_round(round, p);
@@ -673,9 +710,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const int key0 = jb * kBlockN;
         // the block needs a mask iff a key in it lies past the tile's first row or past Nk
         if (key0 + kBlockN - 1 > tile_lim || key0 + kBlockN > p.Nk) {
-          const int lim_causal = row_lim - key0;
-          const int lim_tail = p.Nk - 1 - key0;
-          const int lim = lim_causal < lim_tail ? lim_causal : lim_tail;
+          const int lim = min(row_lim - key0, p.Nk - 1 - key0);  // keys c > lim are masked
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
             if (c > lim) s[c] = -INFINITY;
@@ -765,16 +800,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           tmem_st4(tS + kFp4SfaCol, sa4);
           tmem_st4(tS + kFp4SfbCol, sb4);
         } else {
-          // row max: four independent chains of three-input max
-          float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]), a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
-#pragma unroll
-          for (int c = 8; c < kBlockN; c += 8) {
-            a0 = fmax3(a0, s[c], s[c + 1]);
-            a1 = fmax3(a1, s[c + 2], s[c + 3]);
-            a2 = fmax3(a2, s[c + 4], s[c + 5]);
-            a3 = fmax3(a3, s[c + 6], s[c + 7]);
-          }
-          const float m_blk = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * cj;
+          const float m_blk = row_max128(s) * cj;
           float alpha = 1.f;
           bool moved = false;
           if (m_blk > m_use + kRescaleThreshold) {
@@ -837,9 +863,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         ++pv_iter;
         tc_fence_after();
         const float inv_l = ((kFp8 && !kFp4) ? sv_max * (1.f / 64.f) : 1.f) / l;
-        const size_t r = static_cast<size_t>(bh) * p.Nq + row;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + r * D);
-        // O in 64-column halves (fewer live registers); the last load frees O_t
+        // O in 64-column chunks: each thread writes its row's 128 bytes of bf16
+        // into the tile's staging chunk (the 128-byte swizzle the tensor map
+        // expects, which also keeps the 16-byte stores free of bank conflicts),
+        // one thread stores the chunk with TMA (rows past Nq are clipped), and
+        // the next chunk waits until the store has read the buffer.  The last
+        // TMEM load frees O_t.
+        if constexpr (kTmaO) {
+        const uint32_t stage = sOst + t * Plan::kOstChunkBytes;
+        const uint32_t my_row = stage + row_in_tile * 128;
+        const bool issuer = (threadIdx.x & 127) == 0;
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
           uint32_t oraw[64];
@@ -848,19 +881,61 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             tc_fence_before();
             mbar_arrive(b_o_free + 8 * t);  // the next unit's first P V may overwrite O_t now
           }
-          if (row < p.Nq) {
+          if (ost_uses > 0 &&
+              !(ok = warp_wait(b_ost_free + 8 * t, (ost_uses - 1) & 1, abort_flag, tmo, p.err, 28 + t)))
+            break;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              uint32_t w[4];
+          for (int v = 0; v < 8; ++v) {
+            uint32_t w[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * inv_l,
-                                   __uint_as_float(oraw[8 * v + 2 * e + 1]) * inv_l);
-              dst[8 * h + v] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * inv_l,
+                                 __uint_as_float(oraw[8 * v + 2 * e + 1]) * inv_l);
+            st_shared_v4(my_row + ((v ^ (row_in_tile & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA engine
+          mbar_arrive(b_ost_ready + 8 * t);
+          if (issuer) {
+            ok = mbar_wait(b_ost_ready + 8 * t, ost_uses & 1, abort_flag, tmo, p.err, 30 + t);
+            if (ok) {
+              tma_store_3d(&tmap_o, stage, 64 * h, qt * kBlockM, bh);
+              bulk_commit_group();
+              bulk_wait_read_all();
+              mbar_arrive(b_ost_free + 8 * t);
+            }
+          }
+          ok = __all_sync(0xffffffffu, ok);
+          ++ost_uses;
+          if (!ok) break;
+        }
+        if (!ok) break;
+        } else {
+          const size_t r = static_cast<size_t>(bh) * p.Nq + row;
+          uint4* dst = reinterpret_cast<uint4*>(p.o + r * D);
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            uint32_t oraw[64];
+            tmem_ld64_wait(tO + 64 * h, oraw);
+            if (h == D / 64 - 1) {
+              tc_fence_before();
+              mbar_arrive(b_o_free + 8 * t);
+            }
+            if (row < p.Nq) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * inv_l,
+                                     __uint_as_float(oraw[8 * v + 2 * e + 1]) * inv_l);
+                dst[8 * h + v] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
             }
           }
         }
-        // lse = ln(sum_j exp(scale * s_j)) = ln2 * (m_use + log2(l))
+        // lse = ln(sum_j exp(scale * s_j)) = ln2 * (m_use + log2(l)); consecutive
+        // threads hold consecutive rows, so a warp's stores are contiguous
+        const size_t r = static_cast<size_t>(bh) * p.Nq + row;
         if (row < p.Nq && p.lse != nullptr) p.lse[r] = (m_use + lg2_approx(l)) * 0.69314718055994530942f;
       } else {
         uint32_t oraw[D];
@@ -889,6 +964,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           p.lse_part[rp] = empty ? -INFINITY : (m_use + lg2_approx(l)) * 0.69314718055994530942f;
         }
       }
+    }
+    // the TMA stores of O have completed before the CTA exits
+    if constexpr (kTmaO) {
+      if ((threadIdx.x & 127) == 0) bulk_wait_all();
     }
   }
 
