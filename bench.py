@@ -82,9 +82,10 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_instance(dtype: str, d: int, partial: bool = False) -> str:
+def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = False) -> str:
     """The forward kernel's template instance as ncu names it, read from the
-    instance table of attn_api.cu (D, K stages, V stages, fp8, partial, fp4)."""
+    instance table of attn_api.cu (D, K stages, V stages, fp8, partial, fp4, and
+    the TMA store of O, which the non-causal BF16 launches use)."""
     import re
     text = open(os.path.join(CSRC, "attn_api.cu")).read()
     inst = dict(re.findall(r"#define (ATTN_\w+_D\d+) (\d+, \d+, \d+, (?:true|false))", text))
@@ -93,7 +94,9 @@ def kernel_instance(dtype: str, d: int, partial: bool = False) -> str:
         return "attn::attn_fwd_kernel<?>"
     D, nk, nv, fp8 = (x.strip() for x in inst[key].split(","))
     fp4 = dtype == "e4m3_e2m1"
-    args = [D, nk, nv, "1" if fp8 == "true" else "0", "1" if partial else "0", "1" if fp4 else "0"]
+    tma_o = dtype == "bf16" and not partial and not causal
+    args = [D, nk, nv, "1" if fp8 == "true" else "0", "1" if partial else "0", "1" if fp4 else "0",
+            "1" if tma_o else "0"]
     return "attn::attn_fwd_kernel<" + ", ".join(args) + ">"
 
 
@@ -611,7 +614,7 @@ def main():
     elif decode:
         kname = kernel_instance(w.dtype, w.d, partial=True) + " + attn::attn_merge_kernel"
     else:
-        kname = kernel_instance(w.dtype, w.d)
+        kname = kernel_instance(w.dtype, w.d, causal=w.causal)
     clocks = clk.summary()
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic_for(w.name + (":bwd" if bwd else "")), "peak_source": src,
