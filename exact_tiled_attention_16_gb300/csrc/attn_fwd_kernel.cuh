@@ -33,7 +33,8 @@
 // Synchronisation (mbarriers):
 //   q_full/q_empty        the two Q tiles of a unit (TMA -> MMA -> TMA)
 //   k_full/k_empty[st]    K ring (TMA -> MMA; freed after the last S using it)
-//   v_full/v_empty[st]    V ring (TMA -> MMA, or -> converter for FP8)
+//   v_full/v_empty[st]    V ring (TMA -> MMA, or -> converter for FP8; BF16 frees
+//                         a stage right after tile 1's P V, before the next S)
 //   c_full/c_empty[b]     FP8: f16 copy of V (converter -> MMA -> converter)
 //   s_full[t]   MMA -> softmax: S_t,j ready; since it is committed after
 //               O_t += P_t,j-1 V_j-1, it also means O_t and P_t are free
@@ -42,6 +43,15 @@
 //   p_full[t]   softmax -> MMA: all of P_t,j written
 //   pv_done[t]  MMA -> softmax: the unit's last P_t V product has completed
 //   o_free[t]   softmax -> MMA: the epilogue has read O_t
+//   ost_ready[t], ost_free[t]  (kTmaO) epilogue threads -> the warpgroup's
+//               storing thread: a 64-column chunk of bf16 O_t is in the staging
+//               buffer; storing thread -> epilogue threads: its TMA store has read
+//               the buffer
+//
+// Epilogue: O_t / l to bf16.  kTmaO instances (non-causal BF16 launches) stage
+// each 64-column chunk in shared memory (128-byte swizzle) and store it with one
+// TMA tensor store per chunk (rows past N clipped by the tensor map); the others
+// store each thread's row directly in 16-byte pieces.
 //
 // Block-scaled FP8 variant (kFp8): Q, K, V are e4m3 with one fp32 scale per
 // (batch, head, 128-token block) -- the block quantisation and FP8 tensor-core
@@ -96,6 +106,10 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kRegsLaunch * kNumT
 // at most 2^8, which the 16-bit P and the fp32 accumulators absorb.
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kFp8PScaleLog2 = 6.0f;
+// FP8 stores P' = 2^(x - m + kFp8PScaleLog2 + ...) in f16, with x - m at most the
+// threshold: the largest P' must stay below f16's largest binade (2^15).  (A
+// threshold of 12 overflowed to inf; 8, 12 and 16 ran at the same speed.)
+static_assert(kRescaleThreshold + kFp8PScaleLog2 <= 15.0f, "FP8 P' would overflow f16");
 // Every kPolyEvery-th pair of scores of a row would take its two exponentials
 // from the FMA pipe (exp2_poly2) instead of the special-function unit; 0 = all
 // on the SFU.  Measured on GB300 (doubled SFU ex2 rate), every share is slower:
