@@ -1,9 +1,13 @@
-// Diagnostics of the library: the two ways the softmax can take its
-// exponentials -- ex2.approx on the special-function unit and the FMA-pipe
-// polynomial exp2_poly2 -- evaluated on caller data (for tests against the host's
-// exact 2^x) and timed on the device the caller has current.  The benchmark turns
-// the rates into the special-function-unit ceiling of the forward kernel (one
-// exponential per score against 4 d tensor-core flops per score).
+// Diagnostics of the library.
+//  * The two ways the softmax can take its exponentials -- ex2.approx on the
+//    special-function unit and the FMA-pipe polynomial exp2_poly2 -- evaluated on
+//    caller data (for tests against the host's exact 2^x) and timed on the device
+//    the caller has current.  The benchmark turns the rates into the
+//    special-function-unit ceiling of the forward kernel (one exponential per
+//    score against 4 d tensor-core flops per score).
+//  * The TMEM load with a max reduction that gives the forward kernel its row
+//    maxima (tmem_ld128_max_wait), run on a caller tile so that a test can check
+//    the maximum and the loaded values bit for bit.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -84,7 +88,61 @@ __global__ void diag_eval_kernel(const float* x, float* y_poly, float* y_sfu, lo
   }
 }
 
+// One 128 x 128 f32 tile through TMEM: thread t writes row t of `in` into TMEM
+// lane t, loads it back with tmem_ld128_max_wait and writes the values it got to
+// `vals` and their maximum to `row_max[t]`.  128 threads, one CTA; warp w reaches
+// lanes 32 w .. 32 w + 31.
+__global__ void __launch_bounds__(128, 1) diag_tmem_row_max_kernel(const float* in, float* vals, float* row_max) {
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x / 32;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = tmem_slot + (static_cast<uint32_t>(32 * warp) << 16);
+  const float* src = in + static_cast<size_t>(threadIdx.x) * 128;
+#pragma unroll
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(src[c0 + c]);
+    tmem_st32(taddr + c0, w);
+  }
+  tmem_st_wait();
+  uint32_t r[128];
+  float mx;
+  tmem_ld128_max_wait(taddr, r, mx);
+  float* dst = vals + static_cast<size_t>(threadIdx.x) * 128;
+#pragma unroll
+  for (int c = 0; c < 128; ++c) dst[c] = __uint_as_float(r[c]);
+  row_max[threadIdx.x] = mx;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_slot, 128);
+  }
+}
+
 }  // namespace
+
+extern "C" int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, void* stream) {
+  if (!in || !vals || !row_max) return ATTN_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(vals) | reinterpret_cast<uintptr_t>(row_max)) &
+      3u)
+    return ATTN_ERR_ALIGN;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (major != 10 || minor != 3) return ATTN_ERR_ARCH;
+  diag_tmem_row_max_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(in, vals, row_max);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
 
 extern "C" int attn_eval_exp2(const float* x, float* y_poly, float* y_sfu, long long n, void* stream) {
   if (!x || !y_poly || !y_sfu) return ATTN_ERR_NULL;

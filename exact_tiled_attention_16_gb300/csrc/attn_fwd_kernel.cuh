@@ -48,6 +48,11 @@
 //               buffer; storing thread -> epilogue threads: its TMA store has read
 //               the buffer
 //
+// Row max: the scores come out of TMEM with tcgen05.ld.red .max (a Blackwell
+// Ultra form), which returns each row's maximum with the load, so a block
+// without masked keys spends no instructions on it; masked blocks (the causal
+// diagonal, keys past N) take the maximum of the visible scores in registers.
+//
 // Epilogue: O_t / l to bf16.  kTmaO instances (non-causal BF16 launches) stage
 // each 64-column chunk in shared memory (128-byte swizzle) and store it with one
 // TMA tensor store per chunk (rows past N clipped by the tensor map); the others
@@ -716,7 +721,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         ++s_iter;
         tc_fence_after();
         uint32_t sraw[kBlockN];
-        tmem_ld128_wait(tS, sraw);
+        // the raw scores' row maximum comes with the load (BF16 and FP8)
+        float s_max = -INFINITY;
+        if constexpr (kFp4) tmem_ld128_wait(tS, sraw);
+        else tmem_ld128_max_wait(tS, sraw, s_max);
         float s[kBlockN];
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sraw[c]);
@@ -728,6 +736,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
             if (c > lim) s[c] = -INFINITY;
+          if constexpr (!kFp4) s_max = row_max128(s);  // the maximum over the visible keys
         }
         if constexpr (kFp4) {
           // Direct-P.  Block maxima of the raw scores (cj > 0 keeps the order)
@@ -814,7 +823,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           tmem_st4(tS + kFp4SfaCol, sa4);
           tmem_st4(tS + kFp4SfbCol, sb4);
         } else {
-          const float m_blk = row_max128(s) * cj;
+          const float m_blk = s_max * cj;
           float alpha = 1.f;
           bool moved = false;
           if (m_blk > m_use + kRescaleThreshold) {

@@ -302,6 +302,19 @@ int attn_measure_exp2_rates(float* sfu_per_clk_sm, float* fma_poly_per_clk_sm, v
  */
 int attn_eval_exp2(const float* x, float* y_poly, float* y_sfu, long long n, void* stream);
 
+/*
+ * attn_diag_tmem_row_max -- diagnostics (no counterpart on the pages): passes one
+ * 128 x 128 f32 tile through tensor memory the way the forward kernel reads its
+ * scores.  Row t of `in` is stored into TMEM lane t and loaded back with the
+ * load-with-maximum the softmax uses for its row max (tcgen05.ld.red .max);
+ * vals[t][c] = the loaded values, row_max[t] = the maximum the load returned.
+ * in, vals: device float arrays of 128 x 128 (row-major); row_max: 128 device
+ * floats; all 4-byte aligned.  One CTA of 128 threads that allocates 128 TMEM
+ * columns.  Asynchronous on `stream`.  Returns ATTN_OK, ATTN_ERR_NULL,
+ * ATTN_ERR_ALIGN, ATTN_ERR_ARCH, ATTN_ERR_LAUNCH or ATTN_ERR_CUDA.
+ */
+int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
