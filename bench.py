@@ -82,10 +82,12 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = False) -> str:
+def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = False, table: bool = False) -> str:
     """The forward kernel's template instance as ncu names it, read from the
-    instance table of attn_api.cu (D, K stages, V stages, fp8, partial, fp4, and
-    the TMA store of O, which the non-causal BF16 launches use)."""
+    instance table of attn_api.cu (D, K stages, V stages, fp8, partial, fp4, the
+    TMA store of O, which the non-causal BF16 launches use, and the unit table,
+    which BF16 launches use when every CTA's rounds fit in it: `table`, from the
+    library's schedule diagnostic)."""
     import re
     text = open(os.path.join(CSRC, "attn_api.cu")).read()
     inst = dict(re.findall(r"#define (ATTN_\w+_D\d+) (\d+, \d+, \d+, (?:true|false))", text))
@@ -95,8 +97,9 @@ def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = Fa
     D, nk, nv, fp8 = (x.strip() for x in inst[key].split(","))
     fp4 = dtype == "e4m3_e2m1"
     tma_o = dtype == "bf16" and not partial and not causal
+    tab = dtype == "bf16" and not partial and table
     args = [D, nk, nv, "1" if fp8 == "true" else "0", "1" if partial else "0", "1" if fp4 else "0",
-            "1" if tma_o else "0"]
+            "1" if tma_o else "0", "1" if tab else "0"]
     return "attn::attn_fwd_kernel<" + ", ".join(args) + ">"
 
 
@@ -614,7 +617,12 @@ def main():
     elif decode:
         kname = kernel_instance(w.dtype, w.d, partial=True) + " + attn::attn_merge_kernel"
     else:
-        kname = kernel_instance(w.dtype, w.d, causal=w.causal)
+        table = False
+        if w.dtype == "bf16":
+            table = bool(pkg.diag_fwd_schedule(w.B * w.H, w.N, w.N, w.causal, d=w.d,
+                                               num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+                         [0]["table"])
+        kname = kernel_instance(w.dtype, w.d, causal=w.causal, table=table)
     clocks = clk.summary()
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic_for(w.name + (":bwd" if bwd else "")), "peak_source": src,

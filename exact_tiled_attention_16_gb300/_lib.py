@@ -85,6 +85,11 @@ def load_library():
     lib.attn_eval_exp2.restype = ci
     lib.attn_diag_tmem_row_max.argtypes = [vp, vp, vp, vp]
     lib.attn_diag_tmem_row_max.restype = ci
+    lib.attn_diag_fwd_schedule.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_longlong, ci, ci, vp, vp,
+                                           ctypes.c_longlong]
+    lib.attn_diag_fwd_schedule.restype = ci
+    lib.attn_diag_force_fwd_order.argtypes = [ci, ci]
+    lib.attn_diag_force_fwd_order.restype = ci
     _lib = lib
     return lib
 
@@ -462,3 +467,37 @@ def diag_tmem_row_max(x, stream=None):
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_diag_tmem_row_max")
     return vals, row_max
+
+
+ORDER_HEADS, ORDER_ZIGZAG, ORDER_GROUPS = 0, 1, 2
+
+
+def diag_fwd_schedule(BH, Nq, Nk, causal, d=128, num_sms=152, q_offset=0, k_offset=0, kv_key_bytes=None,
+                      table_ok=True):
+    """The forward kernel's unit schedule for a launch shape (host only, no GPU):
+    (info, seq) with info = {order, group_heads, grid, rounds, makespan, table}
+    and seq an int32 array [grid, rounds] of unit ids (-2: skipped iteration, -1:
+    done).  table_ok: a BF16 attn_fwd launch (True) or another entry point."""
+    import numpy as np
+    kv = 4 * d if kv_key_bytes is None else kv_key_bytes
+    lib = load_library()
+    info = (ctypes.c_int * 6)()
+    args = (BH, Nq, Nk, int(bool(causal)), q_offset, k_offset, kv, int(bool(table_ok)), num_sms)
+    rc = lib.attn_diag_fwd_schedule(*args, ctypes.cast(info, ctypes.c_void_p), None, 0)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_diag_fwd_schedule")
+    grid, rounds = info[2], info[3]
+    seq = np.empty((grid, rounds), dtype=np.int32)
+    rc = lib.attn_diag_fwd_schedule(*args, ctypes.cast(info, ctypes.c_void_p), seq.ctypes.data, seq.size)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_diag_fwd_schedule")
+    keys = ("order", "group_heads", "grid", "rounds", "makespan", "table")
+    return dict(zip(keys, list(info))), seq
+
+
+def diag_force_fwd_order(order=-1, group_heads=0):
+    """Force the unit order of later unsplit causal forward launches (order -1:
+    the library's own choice again)."""
+    rc = load_library().attn_diag_force_fwd_order(order, group_heads)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_diag_force_fwd_order")

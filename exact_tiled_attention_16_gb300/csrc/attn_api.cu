@@ -7,7 +7,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/attn.h"
 #include "attn_fwd_kernel.cuh"
@@ -53,11 +55,12 @@ EncodeTiledFn get_encode() {
   return g_encode;
 }
 
-template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false>
+template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false,
+          bool kTable = false>
 cudaError_t configure_kernel() {
-  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO>,
+  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO, kTable>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO>::kBytes));
+                              static_cast<int>(SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>::kBytes));
 }
 
 // Ring depths (K stages, V stages) per instance; shared memory holds the two Q
@@ -102,6 +105,10 @@ int device_setup(int* dev_out) {
         configure_kernel<ATTN_BF16_D128, false>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D64, false, false, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, false, false, true>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D64, false, false, true, true>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D128, false, false, true, true>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D64, false, false, false, true>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D128, false, false, false, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D64, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, true>() != cudaSuccess ||
         configure_kernel<ATTN_FP8_D128, false>() != cudaSuccess ||
@@ -236,9 +243,152 @@ SplitPlan split_plan(int num_kblocks, int requested) {
   return sp;
 }
 
-// kv_key_bytes: bytes of one key's K and V rows together (sizes the L2 test below)
+// ---------------------------------------------------------------------------
+// Unit order of unsplit causal launches.  Every candidate order is scored by the
+// longest CTA's predicted time, walking the kernel's own schedule functions
+// (unit_for_round, unit_info) with a unit costing max(n0, n1) + 2 K/V block
+// periods (its two tiles advance together; 2 periods of prologue and epilogue).
+// Candidates: zigzag, head-major and -- only for the BF16 instances that read
+// their units from a table (table_cap > 0), where the order's arithmetic costs
+// nothing at run time -- head groups whose K/V together stay under
+// kPairOrderMaxKvBytes (a group of one head is always allowed), at most
+// kMaxGroupCounts group counts.  A table instance takes every CTA's rounds
+// from its table, so an order qualifies for it only when no CTA takes more
+// rounds than the table holds; when none does, the launch goes to the table-less
+// instance with zigzag or head-major order.  Ties keep the earlier candidate
+// (zigzag, head-major, then the smaller groups: fewer bytes of K/V live in L2 at
+// a time).  The choice is cached per shape.
+// ---------------------------------------------------------------------------
+constexpr double kUnitOverheadBlocks = 2.0;
+constexpr int kMaxGroupCounts = 32;
+constexpr long long kNoSearchRounds = 4 * kSchedEntries;  // zigzag's last round then costs < 0.5%
+
+int grid_for(const FwdParams& p, int num_sms) {
+  // work items dealt to CTAs: units, or combined heavy+light pairs under zigzag
+  const int items = p.order == kOrderZigzag ? p.BH * ((p.num_pairs + 1) / 2) : p.num_units;
+  return items < num_sms ? items : num_sms;
+}
+
+// Predicted makespan (K/V block periods) of p's order on num_sms SMs, and the
+// most rounds (iterations, skipped ones included) a CTA takes.
+double predicted_makespan(const FwdParams& p, int num_sms, int* max_rounds = nullptr) {
+  const int G = grid_for(p, num_sms);
+  double worst = 0.0;
+  int rounds = 0;
+  for (int c = 0; c < G; ++c) {
+    double t = 0.0;
+    int round = 0;
+    for (;; ++round) {
+      const int u = unit_for_round(round, p, G, c);
+      if (u == kNoMoreUnits) break;
+      if (u == kSkipRound) continue;
+      const UnitInfo ui = unit_info(u, p);
+      t += (ui.n[1] > ui.n[0] ? ui.n[1] : ui.n[0]) + kUnitOverheadBlocks;
+    }
+    if (t > worst) worst = t;
+    if (round > rounds) rounds = round;
+  }
+  if (max_rounds) *max_rounds = rounds;
+  return worst;
+}
+
+using OrderKey = std::tuple<int, int, int, int, int, int, long long, int>;
+struct OrderChoice {
+  int order, group_heads, table;
+};
+std::map<OrderKey, OrderChoice> g_order_cache;
+std::mutex g_order_mu;
+int g_force_order = -1, g_force_group_heads = 0;  // attn_diag_force_fwd_order
+
+// table_cap: rounds the unit table of the launch's kTable instance holds (0: the
+// entry point has none)
+void choose_order(FwdParams& p, int num_sms, long long kv_key_bytes, int table_cap) {
+  const bool table_ok = table_cap > 0;
+  p.order = kOrderHeads;
+  p.group_heads = p.BH;
+  p.sched_table = 0;
+  if (!p.causal || p.num_splits != 1) {
+    // head-major: ceil(units / grid) rounds
+    const int G = grid_for(p, num_sms);
+    p.sched_table = table_ok && (p.num_units + G - 1) / G <= table_cap ? 1 : 0;
+    return;
+  }
+  int force_order, force_hg;
+  {
+    std::lock_guard<std::mutex> lk(g_order_mu);
+    force_order = g_force_order;
+    force_hg = g_force_group_heads;
+  }
+  if (force_order >= 0) {
+    p.order = force_order;
+    p.group_heads = force_hg > 0 && force_hg < p.BH ? force_hg : p.BH;
+    int rounds = 0;
+    if (table_ok) predicted_makespan(p, num_sms, &rounds);
+    p.sched_table = table_ok && rounds <= table_cap ? 1 : 0;
+    return;
+  }
+  if (p.num_units > kNoSearchRounds * num_sms) {  // many rounds: the tail costs little, skip the search
+    p.order = kOrderZigzag;
+    return;
+  }
+  const OrderKey key{p.BH, p.Nq, p.Nk, p.q_offset, p.k_offset, num_sms, kv_key_bytes, table_cap};
+  {
+    std::lock_guard<std::mutex> lk(g_order_mu);
+    const auto it = g_order_cache.find(key);
+    if (it != g_order_cache.end()) {
+      p.order = it->second.order;
+      p.group_heads = it->second.group_heads;
+      p.sched_table = it->second.table;
+      return;
+    }
+  }
+  FwdParams c = p;
+  // best order with the table (every CTA within table_cap rounds) and without
+  OrderChoice best_tab{-1, p.BH, 1}, best_inl{-1, p.BH, 0};
+  double t_tab = 0.0, t_inl = 0.0;
+  auto consider = [&](int order, int hg) {
+    c.order = order;
+    c.group_heads = hg;
+    int rounds = 0;
+    const double t = predicted_makespan(c, num_sms, &rounds);
+    if (order != kOrderGroups && (best_inl.order < 0 || t < t_inl * (1.0 - 1e-3))) {
+      best_inl = {order, hg, 0};
+      t_inl = t;
+    }
+    if (table_ok && rounds <= table_cap && (best_tab.order < 0 || t < t_tab * (1.0 - 1e-3))) {
+      best_tab = {order, hg, 1};
+      t_tab = t;
+    }
+  };
+  consider(kOrderZigzag, p.BH);
+  consider(kOrderHeads, p.BH);
+  if (table_ok) {
+    const long long head_kv = static_cast<long long>(p.Nk) * kv_key_bytes;
+    int last_hg = 0;
+    for (int groups = p.BH < kMaxGroupCounts ? p.BH : kMaxGroupCounts; groups >= 1; --groups) {
+      const int hg = (p.BH + groups - 1) / groups;  // increasing with fewer groups
+      if (hg == last_hg) continue;
+      last_hg = hg;
+      if (hg > 1 && hg * head_kv > kPairOrderMaxKvBytes) break;
+      consider(kOrderGroups, hg);
+    }
+  }
+  const OrderChoice pick = best_tab.order >= 0 ? best_tab : best_inl;
+  p.order = pick.order;
+  p.group_heads = pick.group_heads;
+  p.sched_table = pick.table;
+  std::lock_guard<std::mutex> lk(g_order_mu);
+  if (g_order_cache.size() >= 4096) g_order_cache.clear();
+  g_order_cache[key] = pick;
+}
+
+// kv_key_bytes: bytes of one key's K and V rows together (sizes the L2 cap of the
+// unit order)
+// table_ok: the launch may go to a kTable instance (the BF16 final-output entry
+// points); the table holds kSchedEntries rounds, kSchedEntriesTma in the
+// instances with the O staging buffers (non-causal)
 void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset, int k_offset, int num_splits,
-                 float scale, int dev, long long kv_key_bytes) {
+                 float scale, int num_sms, long long kv_key_bytes, bool table_ok) {
   std::memset(&p, 0, sizeof(p));
   p.BH = BH;
   p.Nq = Nq;
@@ -252,35 +402,21 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
   p.num_splits = sp.num_splits;
   p.num_units = BH * p.num_pairs * p.num_splits;
   p.causal = causal ? 1 : 0;
-  // zigzag pairing balances causal work but halves the number of items dealt to
-  // CTAs; with fewer than four rounds of them the last, partly empty round costs
-  // more than the balance gains
-  const long long combined = static_cast<long long>(BH) * ((p.num_pairs + 1) / 2);
-  p.order = kOrderHeads;
-  if (causal && p.num_splits == 1) {
-    if (combined >= 4ll * g_dev[dev].num_sms) {
-      p.order = kOrderZigzag;
-    } else if (static_cast<long long>(BH) * Nk * kv_key_bytes <= kPairOrderMaxKvBytes) {
-      // few rounds: deal the units heaviest first across all heads (near-optimal
-      // balance); every head's K/V stays in L2 since all of them fit
-      p.order = kOrderPairs;
-    }
-  }
+  choose_order(p, num_sms, kv_key_bytes, !table_ok ? 0 : (causal ? kSchedEntries : kSchedEntriesTma));
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
-  p.err = g_dev[dev].err_ptr;
 }
 
 // mo: tensor map of the bf16 output O (read only by the kTmaO instances)
-template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false>
+template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false,
+          bool kTable = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
            const FwdParams& p, int dev, void* stream) {
-  // work items dealt to CTAs: units, or combined heavy+light pairs under zigzag
-  const int items = p.order == kOrderZigzag ? p.BH * ((p.num_pairs + 1) / 2) : p.num_units;
-  const int grid = items < g_dev[dev].num_sms ? items : g_dev[dev].num_sms;
-  attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO>
-      <<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO>::kBytes, static_cast<cudaStream_t>(stream)>>>(
-          mq, mk, mv, mo, p);
+  if (static_cast<bool>(p.sched_table) != kTable) return ATTN_ERR_LAUNCH;  // the host's own bookkeeping
+  const int grid = grid_for(p, g_dev[dev].num_sms);
+  attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO, kTable>
+      <<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>::kBytes,
+         static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -302,11 +438,19 @@ int launch_bf16(const void* q, const void* k, const void* v, int d, bool partial
   // against row-per-thread stores); causal ones keep the row stores (the staging
   // buffer cost 3% on B4 H16 N2048 d128 causal, whose units are short).
   if (p.causal) {
+    if (p.sched_table) {
+      if (d == 64) return launch<ATTN_BF16_D64, false, false, false, true>(mq, mk, mv, mq, p, dev, stream);
+      return launch<ATTN_BF16_D128, false, false, false, true>(mq, mk, mv, mq, p, dev, stream);
+    }
     if (d == 64) return launch<ATTN_BF16_D64, false>(mq, mk, mv, mq, p, dev, stream);
     return launch<ATTN_BF16_D128, false>(mq, mk, mv, mq, p, dev, stream);
   }
   CUtensorMap mo;
   if ((rc = make_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, p.Nq, p.BH, 64)) != ATTN_OK) return rc;
+  if (p.sched_table) {
+    if (d == 64) return launch<ATTN_BF16_D64, false, false, true, true>(mq, mk, mv, mo, p, dev, stream);
+    return launch<ATTN_BF16_D128, false, false, true, true>(mq, mk, mv, mo, p, dev, stream);
+  }
   if (d == 64) return launch<ATTN_BF16_D64, false, false, true>(mq, mk, mv, mo, p, dev, stream);
   return launch<ATTN_BF16_D128, false, false, true>(mq, mk, mv, mo, p, dev, stream);
 }
@@ -375,7 +519,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, B * H, N, N, causal, 0, 0, 1, scale, dev, 4ll * d);
+  fill_params(p, B * H, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 4ll * d, true);
+  p.err = g_dev[dev].err_ptr;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   return launch_bf16(q, k, v, d, false, p, dev, stream);
@@ -428,7 +573,8 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
     if (c >= kHostSlots) ck(cudaStreamWaitEvent(sc, hp.out_done[slot], 0));
     if (!ok) break;
     FwdParams p;
-    fill_params(p, hn, N, N, causal, 0, 0, 1, scale, dev, 4ll * d);
+    fill_params(p, hn, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 4ll * d, true);
+    p.err = g_dev[dev].err_ptr;
     p.o = reinterpret_cast<__nv_bfloat16*>(dout);
     p.lse = lse ? dl : nullptr;
     if ((rc = launch_bf16(dq, dk, dv, d, false, p, dev, sc)) != ATTN_OK) return rc;
@@ -465,7 +611,8 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map(&mv, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev, 2ll * d);
+  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 2ll * d, false);
+  p.err = g_dev[dev].err_ptr;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.q_scale = q_scale;
@@ -495,7 +642,8 @@ int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* 
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map_vt4(&mv, vt4, d, N, BH)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, dev, 2ll * d);
+  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 2ll * d, false);
+  p.err = g_dev[dev].err_ptr;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.q_scale = q_scale;
@@ -513,7 +661,8 @@ int attn_fwd_partial(const void* q, const void* k, const void* v, float* o_part,
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, B * H, Nq, Nk, causal, q_offset, k_offset, 1, scale, dev, 4ll * d);
+  fill_params(p, B * H, Nq, Nk, causal, q_offset, k_offset, 1, scale, g_dev[dev].num_sms, 4ll * d, false);
+  p.err = g_dev[dev].err_ptr;
   p.o_part = o_part;
   p.lse_part = lse_part;
   return launch_bf16(q, k, v, d, true, p, dev, stream);
@@ -558,7 +707,8 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
   const int BH = B * H;
   FwdParams p;
   // causal: the queries are the last Nq positions of the Nk keys
-  fill_params(p, BH, Nq, Nk, causal, Nk - Nq, 0, num_splits, scale, dev, 4ll * d);
+  fill_params(p, BH, Nq, Nk, causal, Nk - Nq, 0, num_splits, scale, g_dev[dev].num_sms, 4ll * d, false);
+  p.err = g_dev[dev].err_ptr;
   const long long S = p.num_splits;
   if (workspace_bytes < splitkv_workspace_bytes(BH, Nq, d, S)) return ATTN_ERR_WORKSPACE;
   const long long rows = static_cast<long long>(BH) * Nq;
@@ -692,6 +842,50 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns, int* err) {
   mbar_wait(smem_u32(&bar), 0, &abort_word, timeout_ns, err, 99);
 }
 }  // namespace
+
+extern "C" int attn_diag_force_fwd_order(int order, int group_heads) {
+  if (order < -1 || order > kOrderGroups || group_heads < 0) return ATTN_ERR_DIMS;
+  std::lock_guard<std::mutex> lk(g_order_mu);
+  g_force_order = order;
+  g_force_group_heads = group_heads;
+  return ATTN_OK;
+}
+
+extern "C" int attn_diag_fwd_schedule(int BH, int Nq, int Nk, int causal, int q_offset, int k_offset,
+                                      long long kv_key_bytes, int table_ok, int num_sms, int* info, int* seq,
+                                      long long seq_len) {
+  if (!info) return ATTN_ERR_NULL;
+  if (BH < 1 || Nq < 1 || Nk < 1 || num_sms < 1 || kv_key_bytes < 1) return ATTN_ERR_DIMS;
+  const long long qblocks = (static_cast<long long>(Nq) + kBlockM - 1) / kBlockM;
+  if (Nq >= kMaxSeq || Nk >= kMaxSeq || static_cast<long long>(BH) * qblocks > INT_MAX) return ATTN_ERR_OVERFLOW;
+  FwdParams p;
+  fill_params(p, BH, Nq, Nk, causal, q_offset, k_offset, 1, 1.f, num_sms, kv_key_bytes, table_ok != 0);
+  const int G = grid_for(p, num_sms);
+  int rounds = 0;
+  for (int c = 0; c < G; ++c) {
+    int round = 0;
+    while (unit_for_round(round, p, G, c) != kNoMoreUnits) ++round;
+    if (round > rounds) rounds = round;
+  }
+  info[0] = p.order;
+  info[1] = p.group_heads;
+  info[2] = G;
+  info[3] = rounds;
+  info[4] = static_cast<int>(std::llround(predicted_makespan(p, num_sms)));
+  info[5] = p.sched_table;
+  if (seq) {
+    if (seq_len < static_cast<long long>(G) * rounds) return ATTN_ERR_WORKSPACE;
+    for (int c = 0; c < G; ++c) {
+      bool done = false;
+      for (int r = 0; r < rounds; ++r) {
+        const int u = done ? kNoMoreUnits : unit_for_round(r, p, G, c);
+        done = done || u == kNoMoreUnits;
+        seq[static_cast<long long>(c) * rounds + r] = u;
+      }
+    }
+  }
+  return ATTN_OK;
+}
 
 extern "C" int attn_selftest_wait_timeout(void* stream) {
   int dev = 0;

@@ -146,7 +146,9 @@ struct FwdParams {
   int blocks_per_split;
   int num_units;      // BH * num_pairs * num_splits
   int causal;
-  int order;          // unit order: kOrderHeads, kOrderZigzag or kOrderPairs (below)
+  int order;          // unit order: kOrderHeads, kOrderZigzag or kOrderGroups (below)
+  int group_heads;    // kOrderGroups: heads per group
+  int sched_table;    // launched as a kTable instance (host bookkeeping)
   float scale_log2;   // scale * log2(e)
   const float* q_scale;  // FP8 only: [B*H, num_kblocks] block scales
   const float* k_scale;
@@ -168,9 +170,17 @@ struct TileLayout {
   static_assert(kChunks >= 1, "head dimension too small for the 128-byte swizzle");
 };
 
+// One round of a CTA's schedule, decoded (the unit table in shared memory).
+struct SchedEntry {
+  int u;  // unit id, or kNoMoreUnits / kSkipRound
+  int bh, pair, split, kb0, n0, n1, pad;
+};
+constexpr int kSchedEntries = 64;     // rounds a CTA of a kTable instance may take
+constexpr int kSchedEntriesTma = 48;  // ... of a kTable instance with the O staging buffers
+
 // Shared-memory plan of one instance: Q tiles, K ring, V ring and (FP8) the f16
-// copy of V, then the mbarriers.
-template <int D, int NK, int NV, bool kFp8, bool kFp4 = false, bool kTmaO = false>
+// copy of V, the unit table, then the mbarriers.
+template <int D, int NK, int NV, bool kFp8, bool kFp4 = false, bool kTmaO = false, bool kTable = false>
 struct SmemPlan {
   using In = TileLayout<D, kFp8 ? 1 : 2>;   // Q, K, V as loaded
   using V16 = TileLayout<D, 2>;              // V operand of P V (bf16 or f16)
@@ -185,7 +195,10 @@ struct SmemPlan {
   // swizzle)
   static constexpr uint32_t kOst = kC + kNumConv * V16::kTileBytes;
   static constexpr uint32_t kOstChunkBytes = kBlockM * 128;
-  static constexpr uint32_t kBars = kOst + (kTmaO ? kTilesPerUnit * kOstChunkBytes : 0);
+  // the CTA's unit table (kTable instances: all its rounds, decoded)
+  static constexpr int kSchedN = kTable ? (kTmaO ? kSchedEntriesTma : kSchedEntries) : 0;
+  static constexpr uint32_t kSched = kOst + (kTmaO ? kTilesPerUnit * kOstChunkBytes : 0);
+  static constexpr uint32_t kBars = kSched + kSchedN * sizeof(SchedEntry);
   static constexpr int kNumBars = 18 + 2 * NK + 2 * NV + 2 * kNumConv;
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBars + 8 * kNumBars + 16;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
@@ -196,13 +209,17 @@ struct SmemPlan {
 //                 running units share K/V in L2; under the causal mask each head's
 //                 pairs run from the heaviest (last rows) to the lightest; the
 //                 key-range splits of a pair are adjacent.
-//   kOrderZigzag  causal with many units: heavy+light pairs combined, head-major
-//                 (see unit_for_round).
-//   kOrderPairs   causal with few rounds and every head's K/V small enough to stay
-//                 in L2 together: pair-major, heaviest first, dealt back and forth
-//                 over the CTAs -- close to longest-job-first balance (e.g. 94%
-//                 against 84% for 64 heads of 2048 keys on 152 SMs).
-constexpr int kOrderHeads = 0, kOrderZigzag = 1, kOrderPairs = 2;
+//   kOrderZigzag  causal, unsplit: heavy+light pairs combined, head-major (see
+//                 unit_for_round).
+//   kOrderGroups  causal, unsplit: the heads in groups of group_heads; a group's
+//                 units pair-major, heaviest first, dealt back and forth over the
+//                 CTAs (close to longest-job-first balance); the groups run one
+//                 after another, each starting from the other end of the grid, so
+//                 that the CTAs running at a time share one or two groups' K/V in
+//                 L2.  One group of all heads is plain pair-major order.
+// The host picks the order and the group size by predicting each candidate's
+// balance with the same functions (`unit_for_round`, `unit_info`).
+constexpr int kOrderHeads = 0, kOrderZigzag = 1, kOrderGroups = 2;
 constexpr long long kPairOrderMaxKvBytes = 64ll << 20;
 struct UnitInfo {
   int bh, pair, split;
@@ -210,26 +227,17 @@ struct UnitInfo {
   int n[2];  // K/V blocks tile 0 / tile 1 visit (n[1] >= n[0])
 };
 
-__device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p) {
+__host__ __device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p) {
   UnitInfo ui;
-  if (p.order == kOrderPairs) {
-    // causal, unsplit: all heads' heaviest pair, then all heads' next, ...
-    const int pr = u / p.BH;
-    ui.bh = u - pr * p.BH;
-    ui.split = 0;
-    ui.pair = p.num_pairs - 1 - pr;
-  } else {
-    const int per_head = p.num_pairs * p.num_splits;
-    ui.bh = u / per_head;
-    const int r = u - ui.bh * per_head;
-    const int pr = r / p.num_splits;
-    ui.split = r - pr * p.num_splits;
-    ui.pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
-  }
+  const int per_head = p.num_pairs * p.num_splits;
+  ui.bh = u / per_head;
+  const int r = u - ui.bh * per_head;
+  const int pr = r / p.num_splits;
+  ui.split = r - pr * p.num_splits;
+  ui.pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
   ui.kb0 = ui.split * p.blocks_per_split;
   int kb_end = ui.kb0 + p.blocks_per_split;
   if (kb_end > p.num_kblocks) kb_end = p.num_kblocks;
-#pragma unroll
   for (int t = 0; t < kTilesPerUnit; ++t) {
     int hi = kb_end;
     if (p.causal) {
@@ -248,20 +256,33 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p) {
 constexpr int kNoMoreUnits = -1;
 constexpr int kSkipRound = -2;
 
-// The unit this CTA processes in its `round`-th iteration, kNoMoreUnits when it
-// is done, or kSkipRound for an iteration without a unit (every role skips it).
+// Rounds that grid position cc (of G) takes when U units are dealt back and
+// forth: round r holds unit r G + cc on even rounds and r G + G - 1 - cc on odd.
+__host__ __device__ __forceinline__ int dealt_rounds(int U, int cc, int G) {
+  const int full = U / G;
+  const int off = (full & 1) ? (G - 1 - cc) : cc;
+  return full + (off < U - full * G ? 1 : 0);
+}
+
+// The unit CTA c of a grid of G processes in its `round`-th iteration,
+// kNoMoreUnits when it is done, or kSkipRound for an iteration without a unit
+// (every role skips it).
 //
-// Causal, unsplit: "zigzag" pairing.  Pair p of a head costs about 4p+3 K/V
-// blocks, so the heavy pair P-1-c and the light pair c together cost the same
-// for every c.  Combined unit k = (head, c) goes to CTA k mod G; the CTA runs its
-// heavy pair in the even iteration and its light pair in the odd one (an odd
-// pair count leaves the middle pair alone).  Combined units of one head are
-// adjacent, so the CTAs running at a time share a few heads' K/V in L2.
-// Otherwise: position c of each round on even rounds and the mirror position on
-// odd rounds (the units of a head are adjacent).
-__device__ __forceinline__ int unit_for_round(int round, const FwdParams& p) {
-  const int G = gridDim.x;
-  const int c = blockIdx.x;
+// kOrderZigzag: pair p of a head costs about 4p+3 K/V blocks, so the heavy pair
+// P-1-k and the light pair k together cost the same for every k.  Combined unit
+// j = (head, k) goes to CTA j mod G; the CTA runs its heavy pair in the even
+// iteration and its light pair in the odd one (an odd pair count leaves the
+// middle pair alone).  Combined units of one head are adjacent, so the CTAs
+// running at a time share a few heads' K/V in L2.
+// kOrderGroups: group g (heads g Hg ..) holds Hg P units, position q = pr Hg + h
+// for the pr-th heaviest pair of its h-th head; the group is dealt back and forth
+// from grid position c (even groups) or G - 1 - c (odd groups), so CTA c takes
+// dealt_rounds(.., c) + dealt_rounds(.., G - 1 - c) rounds per two full groups.
+// kOrderHeads: position c of each round on even rounds and the mirror position
+// on odd rounds (the units of a head are adjacent).
+// kGroups = false leaves kOrderGroups out (instances that never run it).
+template <bool kGroups = true>
+__host__ __device__ __forceinline__ int unit_for_round(int round, const FwdParams& p, int G, int c) {
   if (p.order == kOrderZigzag) {
     const int half = (p.num_pairs + 1) >> 1;
     const int k = (round >> 1) * G + c;
@@ -273,8 +294,55 @@ __device__ __forceinline__ int unit_for_round(int round, const FwdParams& p) {
     const int pair = (round & 1) ? cc : heavy;
     return bh * p.num_pairs + (p.num_pairs - 1 - pair);  // unit id as unit_info decodes it
   }
+  if (kGroups && p.order == kOrderGroups) {
+    const int hg = p.group_heads;
+    const int num_groups = (p.BH + hg - 1) / hg;
+    const int full_units = hg * p.num_pairs;
+    const int n0 = dealt_rounds(full_units, c, G), n1 = dealt_rounds(full_units, G - 1 - c, G);
+    if (n0 + n1 == 0) return kNoMoreUnits;
+    int g = 2 * (round / (n0 + n1));
+    int r = round - (g >> 1) * (n0 + n1);
+    if (r >= n0) {
+      r -= n0;
+      ++g;
+    }
+    if (g >= num_groups) return kNoMoreUnits;
+    const int heads = (p.BH - g * hg) < hg ? (p.BH - g * hg) : hg;  // the last group may be smaller
+    const int cc = (g & 1) ? (G - 1 - c) : c;
+    if (heads < hg && r >= dealt_rounds(heads * p.num_pairs, cc, G)) return kNoMoreUnits;
+    const int q = r * G + ((r & 1) ? (G - 1 - cc) : cc);
+    const int pr = q / heads;  // 0: the heaviest pair
+    const int bh = g * hg + (q - pr * heads);
+    return bh * p.num_pairs + pr;
+  }
   const int pos = round * G + ((round & 1) ? (G - 1 - c) : c);
   return pos < p.num_units ? pos : kNoMoreUnits;
+}
+
+// The unit of the CTA's `round`-th iteration and its decoded info.  kTable
+// instances (kN > 0) read it from the table the CTA fills in its prologue (all
+// threads, one round each), so that no role spends the schedule's integer
+// divisions on its path from one unit to the next; the host launches them only
+// when every CTA's rounds fit in the table.  The others compute it here, and
+// the host gives them only the head-major and zigzag orders, whose arithmetic
+// is short.
+template <int kN>
+__device__ __forceinline__ int next_unit(int round, const SchedEntry* tab, const FwdParams& p, UnitInfo& ui) {
+  if constexpr (kN > 0) {
+    if (round >= kN) return kNoMoreUnits;
+    const SchedEntry e = tab[round];
+    ui.bh = e.bh;
+    ui.pair = e.pair;
+    ui.split = e.split;
+    ui.kb0 = e.kb0;
+    ui.n[0] = e.n0;
+    ui.n[1] = e.n1;
+    return e.u;
+  } else {
+    const int u = unit_for_round<false>(round, p, gridDim.x, blockIdx.x);
+    if (u >= 0) ui = unit_info(u, p);
+    return u;
+  }
 }
 
 // Largest of 128 scores: four independent chains of three-input max.
@@ -312,14 +380,15 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // lse, where a tile or row may see no key at all.  kTmaO (final bf16 output
 // only): O leaves through shared-memory staging and TMA stores instead of
 // row-per-thread global stores.
-template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false>
+template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false,
+          bool kTable = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
                 const FwdParams p) {
   static_assert(!kFp4 || (kFp8 && D == 128 && !kPartial), "Direct-P FP4: e4m3 Q K^T, d = 128, final output");
   static_assert(!kTmaO || !kPartial, "the TMA store serves the final bf16 output");
-  using Plan = SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO>;
+  using Plan = SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>;
   using L = typename Plan::In;
   using LV = typename Plan::V16;
   constexpr uint32_t kTmemS[2] = {0, 128};
@@ -398,6 +467,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  SchedEntry* sched = reinterpret_cast<SchedEntry*>(smem + Plan::kSched);
+  for (int i = threadIdx.x; i < Plan::kSchedN; i += kNumThreads) {
+    SchedEntry e{};
+    e.u = unit_for_round(i, p, gridDim.x, blockIdx.x);
+    if (e.u >= 0) {
+      const UnitInfo ui = unit_info(e.u, p);
+      e.bh = ui.bh;
+      e.pair = ui.pair;
+      e.split = ui.split;
+      e.kb0 = ui.kb0;
+      e.n0 = ui.n[0];
+      e.n1 = ui.n[1];
+    }
+    sched[i] = e;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -413,10 +497,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       int units = 0, q_issued = 0;  // units with work, Q loads issued
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round, p);
+        UnitInfo ui;
+        const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
         if (u == kNoMoreUnits) break;
         if (u == kSkipRound) continue;
-        const UnitInfo ui = unit_info(u, p);
         const int nkv = ui.n[1];
         if (nkv == 0) continue;  // no visible keys: the softmax warps write the empty result
         if (units > 0 && !(ok = mbar_wait(b_q_empty, (units - 1) & 1, abort_flag, tmo, p.err, 1))) break;
@@ -524,10 +608,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       };
       int o_uses[2] = {0, 0};  // units in which tile t has written O_t
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round, p);
+        UnitInfo ui;
+        const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
         if (u == kNoMoreUnits) break;
         if (u == kSkipRound) continue;
-        const UnitInfo ui = unit_info(u, p);
         const int n0 = ui.n[0], n1 = ui.n[1];
         if (n1 == 0) continue;
         if (!(ok = warp_wait(b_q_full, units & 1, abort_flag, tmo, p.err, 10))) break;
@@ -621,10 +705,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       uint32_t g = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
-        const int u = unit_for_round(round, p);
+        UnitInfo ui;
+        const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
         if (u == kNoMoreUnits) break;
         if (u == kSkipRound) continue;
-        const int nkv = unit_info(u, p).n[1];
+        const int nkv = ui.n[1];
         for (int j = 0; j < nkv && ok; ++j, ++g) {
           const uint32_t sv = g % NV, b = g & 1;
           if (!(ok = mbar_wait(b_v_full + 8 * sv, (g / NV) & 1, abort_flag, tmo, p.err, 30))) break;
@@ -669,10 +754,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     uint32_t ost_uses = 0;  // TMA stores of O issued from this tile's staging chunk
     bool ok = true;
     for (int round = 0; ok; ++round) {
-      const int u = unit_for_round(round, p);
+      UnitInfo ui;
+      const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
       if (u == kNoMoreUnits) break;
       if (u == kSkipRound) continue;
-      const UnitInfo ui = unit_info(u, p);
       const int bh = ui.bh;
       const int qt = 2 * ui.pair + t;
       const int nkv = t == 0 ? ui.n[0] : ui.n[1];

@@ -315,6 +315,44 @@ int attn_eval_exp2(const float* x, float* y_poly, float* y_sfu, long long n, voi
  */
 int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, void* stream);
 
+/*
+ * attn_diag_fwd_schedule -- diagnostics (no counterpart on the pages; host only,
+ * no GPU work): the order in which the forward kernel's persistent CTAs take
+ * their work units for a launch of BH heads of Nq query rows over Nk keys
+ * (causal: 0/1; q_offset, k_offset: positions of the first query row and key,
+ * as in attn_fwd_partial; kv_key_bytes: bytes of one key's K and V rows, 4 d for
+ * BF16, 2 d for e4m3) on num_sms SMs, one key range per unit.  table_ok: 1 for
+ * a launch of attn_fwd / attn_fwd_host (BF16), whose causal launches may take
+ * their units from a table in shared memory and then use any order; 0 for the
+ * other entry points (head-major or zigzag only).
+ * A unit is a pair of 128-row query tiles of one head: id = head * P + r with
+ * P = ceil(Nq / 256) pairs per head; under the causal mask r = 0 is the heaviest
+ * pair (the last rows), otherwise the first.
+ * info (host, 6 ints): [0] order (0 head-major, 1 zigzag, 2 head groups), [1]
+ * heads per group, [2] CTAs launched, [3] rounds: the most iterations a CTA
+ * takes, [4] the predicted time of the busiest CTA in K/V block periods, [5] 1
+ * if the launch takes its units from the table.
+ * seq (host, may be NULL): CTAs x rounds ints, seq[c * rounds + r] = the unit CTA
+ * c takes in its r-th iteration, -2 for an iteration it skips, -1 once it is
+ * done; seq_len: its capacity in ints (else ATTN_ERR_WORKSPACE).
+ * Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_DIMS, ATTN_ERR_OVERFLOW or
+ * ATTN_ERR_WORKSPACE.
+ */
+int attn_diag_fwd_schedule(int BH, int Nq, int Nk, int causal, int q_offset, int k_offset, long long kv_key_bytes,
+                           int table_ok, int num_sms, int* info, int* seq, long long seq_len);
+
+/*
+ * attn_diag_force_fwd_order -- diagnostics (no counterpart on the pages): makes
+ * every later unsplit causal forward launch of this process use the given order
+ * (0 head-major, 1 zigzag, 2 head groups of group_heads heads, 0 = all heads in
+ * one group) instead of the one the library predicts to balance best; order -1
+ * restores the automatic choice.  For tests that run each order on the GPU: a
+ * forced order runs from the unit table when the launch qualifies for one (see
+ * attn_diag_fwd_schedule), else computed by every role.
+ * Returns ATTN_OK or ATTN_ERR_DIMS.
+ */
+int attn_diag_force_fwd_order(int order, int group_heads);
+
 #ifdef __cplusplus
 }
 #endif

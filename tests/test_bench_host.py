@@ -16,13 +16,19 @@ import bench  # noqa: E402
 def test_kernel_instance_follows_the_instance_table():
     text = open(os.path.join(bench.CSRC, "attn_api.cu")).read()
     assert "#define ATTN_BF16_D128 128, 2, 2, false" in text
-    # D, K stages, V stages, fp8, partial, fp4, TMA store of O (non-causal BF16 only)
-    assert bench.kernel_instance("bf16", 128, causal=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0>"
-    assert bench.kernel_instance("bf16", 128, causal=False) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 1>"
-    assert bench.kernel_instance("bf16", 64, causal=False) == "attn::attn_fwd_kernel<64, 4, 4, 0, 0, 0, 1>"
-    assert bench.kernel_instance("bf16", 128, partial=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 1, 0, 0>"
-    assert bench.kernel_instance("e4m3", 128) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0>"
-    assert bench.kernel_instance("e4m3_e2m1", 128) == "attn::attn_fwd_kernel<128, 4, 4, 1, 0, 1, 0>"
+    # D, K stages, V stages, fp8, partial, fp4, TMA store of O (non-causal BF16 only),
+    # unit table (BF16 launches whose rounds fit in it)
+    assert bench.kernel_instance("bf16", 128, causal=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 0>"
+    assert (bench.kernel_instance("bf16", 128, causal=True, table=True)
+            == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 1>")
+    assert bench.kernel_instance("bf16", 128, causal=False) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 1, 0>"
+    assert bench.kernel_instance("bf16", 64, causal=False) == "attn::attn_fwd_kernel<64, 4, 4, 0, 0, 0, 1, 0>"
+    assert (bench.kernel_instance("bf16", 64, causal=False, table=True)
+            == "attn::attn_fwd_kernel<64, 4, 4, 0, 0, 0, 1, 1>")
+    assert bench.kernel_instance("bf16", 128, partial=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 1, 0, 0, 0>"
+    assert bench.kernel_instance("e4m3", 128) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0>"
+    assert bench.kernel_instance("e4m3_e2m1", 128) == "attn::attn_fwd_kernel<128, 4, 4, 1, 0, 1, 0, 0>"
+    assert bench.kernel_instance("e4m3", 128, causal=True, table=True) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0>"
 
 
 def test_kernel_hash_covers_every_cuda_source(tmp_path, monkeypatch):

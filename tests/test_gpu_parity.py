@@ -192,43 +192,56 @@ def test_torch_streams():
                                  lse.cpu().numpy().astype(np.float64)), "side stream")
 
 
-@pytest.mark.parametrize("shape", [(8, 76, 512, 128), (4, 76, 640, 64)], ids=["pairs2", "pairs3_odd"])
-def test_zigzag_schedule_covers_every_unit(shape):
-    """Causal launches with at least four rounds of combined heavy+light pair
-    units take the zigzag schedule; every row must be written and correct (an
-    odd pair count leaves the middle pair of each head on its own)."""
-    import exact_tiled_attention_16_gb300 as pkg
-    B, H, N, d = shape
-    w = synth.make_bf16(B, H, N, d, True, seed=77 + N)
-    q, k, v = to_device(w)
-    o = torch.full_like(q, float("nan"))
-    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
-    pkg.attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse)
-    torch.cuda.synchronize()
-    assert not torch.isnan(o.float()).any() and not torch.isnan(lse).any()
-    assert_bf16_tol(compare_rows(w, o.float().cpu().numpy().astype(np.float64),
-                                 lse.cpu().numpy().astype(np.float64)), f"zigzag {shape}")
+ORDER_CASES = [(0, 0), (1, 0), (2, 1), (2, 3), (2, 0)]
 
 
-@pytest.mark.parametrize("shape", [(2, 76, 640, 128), (3, 50, 1024, 64), (1, 7, 2304, 128), (2, 40, 777, 64)],
-                         ids=["pairs3_odd_3rounds", "pairs4_d64", "few_heads_ragged_rounds", "ragged_tail_d64"])
-def test_pair_order_schedule_covers_every_unit(shape):
-    """Causal launches with fewer than four rounds of combined units and every
-    head's K/V small enough for L2 take the pair-major order (all heads'
-    heaviest pair first, dealt back and forth over the CTAs); every row must be
-    written and correct, including heads whose pairs land on different CTAs in
-    different rounds."""
+@pytest.mark.parametrize("order", ORDER_CASES, ids=["heads", "zigzag", "groups1", "groups3", "groups_all"])
+@pytest.mark.parametrize("shape", [(2, 76, 640, 128), (3, 50, 1024, 64), (1, 7, 2304, 128), (2, 40, 777, 64),
+                                   (8, 76, 512, 128)],
+                         ids=["pairs3_odd", "pairs4_d64", "few_heads_9pairs", "ragged_tail_d64", "pairs2_many_rounds"])
+def test_every_unit_order_covers_every_unit(shape, order):
+    """Each unit order of causal launches forced in turn (head-major, zigzag with
+    heavy+light pairs combined, head groups of one, of three -- a smaller last
+    group when the head count is not a multiple -- and of all heads): every row
+    must be written and correct, including odd pair counts (the middle pair of a
+    zigzag head alone), ragged last pairs and heads whose pairs land on different
+    CTAs in different rounds."""
     import exact_tiled_attention_16_gb300 as pkg
     B, H, N, d = shape
     w = synth.make_bf16(B, H, N, d, True, seed=91 + N)
     q, k, v = to_device(w)
     o = torch.full_like(q, float("nan"))
     lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
-    pkg.attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse)
-    torch.cuda.synchronize()
+    pkg.diag_force_fwd_order(*order)
+    try:
+        info, _ = pkg.diag_fwd_schedule(B * H, N, N, True, d=d, num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+        assert info["order"] == order[0]
+        pkg.attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse)
+        torch.cuda.synchronize()
+    finally:
+        pkg.diag_force_fwd_order(-1)
     assert not torch.isnan(o.float()).any() and not torch.isnan(lse).any()
     assert_bf16_tol(compare_rows(w, o.float().cpu().numpy().astype(np.float64),
-                                 lse.cpu().numpy().astype(np.float64)), f"pair order {shape}")
+                                 lse.cpu().numpy().astype(np.float64)), f"order {order} {shape}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_instances_past_the_unit_table(causal):
+    """2560 heads of 1024 rows (10240 units, 68 rounds of 152 CTAs): more rounds
+    than the unit table holds (48 beside the non-causal O staging buffers, 64
+    otherwise), so the launch runs the table-less instance that computes every
+    unit on each role (head-major or zigzag order); sampled rows of every head."""
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d = 64, 40, 1024, 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    info, _ = pkg.diag_fwd_schedule(B * H, N, N, causal, d=d, num_sms=sms)
+    if info["rounds"] <= 64:
+        pytest.skip(f"{sms} SMs: every CTA's rounds fit in the table")
+    assert info["table"] == 0
+    w = synth.make_bf16(B, H, N, d, causal, seed=5150 + causal)
+    o, lse = run_bf16(w)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert_bf16_tol(compare_rows(w, o, lse, rows_per_head=8), f"untabled causal={causal}")
 
 
 def _sweep_shapes():
