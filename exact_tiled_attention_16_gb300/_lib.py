@@ -83,7 +83,7 @@ def load_library():
     lib.attn_measure_exp2_rates.restype = ci
     lib.attn_eval_exp2.argtypes = [vp, vp, vp, ctypes.c_longlong, vp]
     lib.attn_eval_exp2.restype = ci
-    lib.attn_diag_tmem_row_max.argtypes = [vp, vp, vp, vp]
+    lib.attn_diag_tmem_row_max.argtypes = [vp, vp, vp, vp, vp]
     lib.attn_diag_tmem_row_max.restype = ci
     lib.attn_diag_fwd_schedule.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.c_longlong, ci, ci, vp, vp,
                                            ctypes.c_longlong]
@@ -454,19 +454,21 @@ def eval_exp2(x, stream=None):
 
 
 def diag_tmem_row_max(x, stream=None):
-    """(vals, row_max) for a contiguous CUDA float32 tensor x of shape (128, 128):
-    the tile passed through tensor memory and loaded back with the load-with-
-    maximum the forward kernel uses for its row maxima."""
+    """(vals, row_max, block_max) for a contiguous CUDA float32 tensor x of shape
+    (128, 128): the tile passed through tensor memory and loaded back with the
+    loads-with-maximum the forward kernel uses (the row's, and each 32-column
+    group's)."""
     import torch
     if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous() or tuple(x.shape) != (128, 128):
         raise ValueError("x must be a contiguous CUDA float32 tensor of shape (128, 128)")
     vals = torch.empty_like(x)
     row_max = torch.empty(128, dtype=torch.float32, device=x.device)
+    block_max = torch.empty((128, 4), dtype=torch.float32, device=x.device)
     rc = load_library().attn_diag_tmem_row_max(x.data_ptr(), vals.data_ptr(), row_max.data_ptr(),
-                                               _stream_handle(stream) or None)
+                                               block_max.data_ptr(), _stream_handle(stream) or None)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_diag_tmem_row_max")
-    return vals, row_max
+    return vals, row_max, block_max
 
 
 ORDER_HEADS, ORDER_ZIGZAG, ORDER_GROUPS = 0, 1, 2

@@ -90,9 +90,11 @@ __global__ void diag_eval_kernel(const float* x, float* y_poly, float* y_sfu, lo
 
 // One 128 x 128 f32 tile through TMEM: thread t writes row t of `in` into TMEM
 // lane t, loads it back with tmem_ld128_max_wait and writes the values it got to
-// `vals` and their maximum to `row_max[t]`.  128 threads, one CTA; warp w reaches
-// lanes 32 w .. 32 w + 31.
-__global__ void __launch_bounds__(128, 1) diag_tmem_row_max_kernel(const float* in, float* vals, float* row_max) {
+// `vals` and their maximum to `row_max[t]`; then with tmem_ld128_max32_wait, the
+// maxima of its four groups of 32 columns to block_max[4 t ..] (if not null).
+// 128 threads, one CTA; warp w reaches lanes 32 w .. 32 w + 31.
+__global__ void __launch_bounds__(128, 1) diag_tmem_row_max_kernel(const float* in, float* vals, float* row_max,
+                                                                   float* block_max) {
   __shared__ uint32_t tmem_slot;
   const int warp = threadIdx.x / 32;
   if (warp == 0) {
@@ -119,6 +121,12 @@ __global__ void __launch_bounds__(128, 1) diag_tmem_row_max_kernel(const float* 
 #pragma unroll
   for (int c = 0; c < 128; ++c) dst[c] = __uint_as_float(r[c]);
   row_max[threadIdx.x] = mx;
+  if (block_max) {
+    float bm[4];
+    tmem_ld128_max32_wait(taddr, r, bm);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) block_max[4 * threadIdx.x + b] = bm[b];
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -129,9 +137,11 @@ __global__ void __launch_bounds__(128, 1) diag_tmem_row_max_kernel(const float* 
 
 }  // namespace
 
-extern "C" int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, void* stream) {
+extern "C" int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, float* block_max,
+                                      void* stream) {
   if (!in || !vals || !row_max) return ATTN_ERR_NULL;
-  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(vals) | reinterpret_cast<uintptr_t>(row_max)) &
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(vals) | reinterpret_cast<uintptr_t>(row_max) |
+       reinterpret_cast<uintptr_t>(block_max)) &
       3u)
     return ATTN_ERR_ALIGN;
   int dev = 0, major = 0, minor = 0;
@@ -140,7 +150,7 @@ extern "C" int attn_diag_tmem_row_max(const float* in, float* vals, float* row_m
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return ATTN_ERR_CUDA;
   if (major != 10 || minor != 3) return ATTN_ERR_ARCH;
-  diag_tmem_row_max_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(in, vals, row_max);
+  diag_tmem_row_max_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(in, vals, row_max, block_max);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

@@ -806,9 +806,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         ++s_iter;
         tc_fence_after();
         uint32_t sraw[kBlockN];
-        // the raw scores' row maximum comes with the load (BF16 and FP8)
+        // the raw scores' maxima come with the load: the row's (BF16 and FP8) or each
+        // 32-key block's (Direct-P FP4)
         float s_max = -INFINITY;
-        if constexpr (kFp4) tmem_ld128_wait(tS, sraw);
+        float bm[4];  // FP4: block maxima of the raw scores (cj > 0 keeps the order)
+        if constexpr (kFp4) tmem_ld128_max32_wait(tS, sraw, bm);
         else tmem_ld128_max_wait(tS, sraw, s_max);
         float s[kBlockN];
 #pragma unroll
@@ -821,21 +823,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
             if (c > lim) s[c] = -INFINITY;
-          if constexpr (!kFp4) s_max = row_max128(s);  // the maximum over the visible keys
+          // the maxima over the visible keys
+          if constexpr (kFp4) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              float g4[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float* x = s + 32 * b + 8 * q;
+                g4[q] = fmaxf(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], fmax3(x[5], x[6], x[7])));
+              }
+              bm[b] = fmaxf(fmaxf(g4[0], g4[1]), fmaxf(g4[2], g4[3]));
+            }
+          } else {
+            s_max = row_max128(s);
+          }
         }
         if constexpr (kFp4) {
-          // Direct-P.  Block maxima of the raw scores (cj > 0 keeps the order)
-          float bm[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            float g4[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float* x = s + 32 * b + 8 * q;
-              g4[q] = fmaxf(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], fmax3(x[5], x[6], x[7])));
-            }
-            bm[b] = fmaxf(fmaxf(g4[0], g4[1]), fmaxf(g4[2], g4[3]));
-          }
+          // Direct-P.
           // E_b = ceil(max t) (base 2; -inf for a block without a visible key)
           float eb[4];
 #pragma unroll

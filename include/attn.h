@@ -307,13 +307,16 @@ int attn_eval_exp2(const float* x, float* y_poly, float* y_sfu, long long n, voi
  * 128 x 128 f32 tile through tensor memory the way the forward kernel reads its
  * scores.  Row t of `in` is stored into TMEM lane t and loaded back with the
  * load-with-maximum the softmax uses for its row max (tcgen05.ld.red .max);
- * vals[t][c] = the loaded values, row_max[t] = the maximum the load returned.
+ * vals[t][c] = the loaded values, row_max[t] = the maximum the load returned;
+ * block_max[t][b] (may be NULL) = the maxima of columns 32 b .. 32 b + 31 from
+ * the four-group form the Direct-P FP4 softmax uses.
  * in, vals: device float arrays of 128 x 128 (row-major); row_max: 128 device
- * floats; all 4-byte aligned.  One CTA of 128 threads that allocates 128 TMEM
- * columns.  Asynchronous on `stream`.  Returns ATTN_OK, ATTN_ERR_NULL,
- * ATTN_ERR_ALIGN, ATTN_ERR_ARCH, ATTN_ERR_LAUNCH or ATTN_ERR_CUDA.
+ * floats; block_max: 128 x 4 device floats; all 4-byte aligned.  One CTA of 128
+ * threads that allocates 128 TMEM columns.  Asynchronous on `stream`.  Returns
+ * ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_ALIGN, ATTN_ERR_ARCH, ATTN_ERR_LAUNCH or
+ * ATTN_ERR_CUDA.
  */
-int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, void* stream);
+int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, float* block_max, void* stream);
 
 /*
  * attn_diag_fwd_schedule -- diagnostics (no counterpart on the pages; host only,

@@ -1,8 +1,9 @@
-"""The TMEM load with a max reduction (tcgen05.ld.red .max) that gives the forward
-kernel its row maxima.  A wrong maximum would not show in the attention parity
-tests -- the softmax does not depend on the shift as long as nothing overflows --
-so the load is checked here on its own, through the library's diagnostic entry
-point: the values it returns and their maximum, bit for bit against the host."""
+"""The TMEM loads with a max reduction (tcgen05.ld.red .max) that give the forward
+kernel its row maxima (BF16, FP8) and its 32-key block maxima (Direct-P FP4).  A
+wrong maximum would not show in the attention parity tests -- the softmax does not
+depend on the shift as long as nothing overflows -- so the loads are checked here
+on their own, through the library's diagnostic entry point: the values they return
+and the maxima, bit for bit against the host."""
 import numpy as np
 import pytest
 
@@ -43,15 +44,19 @@ def _tile(seed):
 def test_load_with_max_returns_the_row_and_its_maximum(seed):
     import exact_tiled_attention_16_gb300 as pkg
     x = _tile(seed)
-    vals, mx = pkg.diag_tmem_row_max(torch.from_numpy(x).cuda())
+    vals, mx, bmx = pkg.diag_tmem_row_max(torch.from_numpy(x).cuda())
     torch.cuda.synchronize()
     vals = vals.cpu().numpy()
     mx = mx.cpu().numpy()
+    bmx = bmx.cpu().numpy()
     assert np.array_equal(vals.view(np.uint32), x.view(np.uint32)), "the loaded values differ from the stored ones"
     want = x.max(axis=1)
     bad = np.nonzero(mx.view(np.uint32) != want.view(np.uint32))[0]
     assert bad.size == 0, f"rows {bad[:8].tolist()}: got {mx[bad[:8]].tolist()}, want {want[bad[:8]].tolist()}"
     assert mx[47] == -np.inf
+    # the four-group form (Direct-P FP4): each 32-column group's maximum
+    want_b = x.reshape(128, 4, 32).max(axis=2)
+    assert np.array_equal(bmx.view(np.uint32), want_b.view(np.uint32)), "a 32-column group maximum differs"
 
 
 def test_rejects_bad_arguments():
