@@ -14,7 +14,7 @@ __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_fp8", "attn_fwd_fp8_raw", "attn
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
            "attn_bwd", "attn_bwd_raw", "bwd_workspace_bytes",
            "check_device_errors", "set_wait_timeout_ns", "selftest_wait_timeout", "measure_exp2_rates", "eval_exp2",
-           "diag_tmem_row_max", "diag_fwd_schedule", "diag_force_fwd_order",
+           "diag_tmem_row_max", "diag_fwd_schedule", "diag_force_fwd_order", "diag_set_pair_tail",
            "ORDER_HEADS", "ORDER_ZIGZAG", "ORDER_GROUPS"]
 
 

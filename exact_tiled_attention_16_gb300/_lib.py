@@ -90,6 +90,8 @@ def load_library():
     lib.attn_diag_fwd_schedule.restype = ci
     lib.attn_diag_force_fwd_order.argtypes = [ci, ci]
     lib.attn_diag_force_fwd_order.restype = ci
+    lib.attn_diag_set_pair_tail.argtypes = [ci]
+    lib.attn_diag_set_pair_tail.restype = ci
     _lib = lib
     return lib
 
@@ -477,13 +479,14 @@ ORDER_HEADS, ORDER_ZIGZAG, ORDER_GROUPS = 0, 1, 2
 def diag_fwd_schedule(BH, Nq, Nk, causal, d=128, num_sms=152, q_offset=0, k_offset=0, kv_key_bytes=None,
                       table_ok=True):
     """The forward kernel's unit schedule for a launch shape (host only, no GPU):
-    (info, seq) with info = {order, group_heads, grid, rounds, makespan, table}
-    and seq an int32 array [grid, rounds] of unit ids (-2: skipped iteration, -1:
-    done).  table_ok: a BF16 attn_fwd launch (True) or another entry point."""
+    (info, seq) with info = {order, group_heads, grid, rounds, makespan, table,
+    pair_tail} and seq an int32 array [grid, rounds] of unit ids (-3 - unit: the
+    odd CTA of a split pair-tail unit, -2: skipped iteration, -1: done).
+    table_ok: a BF16 attn_fwd launch (True) or another entry point."""
     import numpy as np
     kv = 4 * d if kv_key_bytes is None else kv_key_bytes
     lib = load_library()
-    info = (ctypes.c_int * 6)()
+    info = (ctypes.c_int * 7)()
     args = (BH, Nq, Nk, int(bool(causal)), q_offset, k_offset, kv, int(bool(table_ok)), num_sms)
     rc = lib.attn_diag_fwd_schedule(*args, ctypes.cast(info, ctypes.c_void_p), None, 0)
     if rc != ATTN_OK:
@@ -493,7 +496,7 @@ def diag_fwd_schedule(BH, Nq, Nk, causal, d=128, num_sms=152, q_offset=0, k_offs
     rc = lib.attn_diag_fwd_schedule(*args, ctypes.cast(info, ctypes.c_void_p), seq.ctypes.data, seq.size)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_diag_fwd_schedule")
-    keys = ("order", "group_heads", "grid", "rounds", "makespan", "table")
+    keys = ("order", "group_heads", "grid", "rounds", "makespan", "table", "pair_tail")
     return dict(zip(keys, list(info))), seq
 
 
@@ -503,3 +506,9 @@ def diag_force_fwd_order(order=-1, group_heads=0):
     rc = load_library().attn_diag_force_fwd_order(order, group_heads)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_diag_force_fwd_order")
+
+
+def diag_set_pair_tail(enable=True):
+    """Enable or disable the split of the last, partly filled round over CTA pairs
+    for later launches of this process."""
+    load_library().attn_diag_set_pair_tail(1 if enable else 0)

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -56,9 +57,9 @@ EncodeTiledFn get_encode() {
 }
 
 template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false,
-          bool kTable = false>
+          bool kTable = false, bool kPairTail = false>
 cudaError_t configure_kernel() {
-  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO, kTable>,
+  return cudaFuncSetAttribute(attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO, kTable, kPairTail>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>::kBytes));
 }
@@ -106,6 +107,8 @@ int device_setup(int* dev_out) {
         configure_kernel<ATTN_BF16_D64, false, false, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, false, false, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D64, false, false, true, true>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D64, false, false, true, true, true>() != cudaSuccess ||
+        configure_kernel<ATTN_BF16_D128, false, false, true, true, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, false, false, true, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D64, false, false, false, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, false, false, false, true>() != cudaSuccess ||
@@ -262,8 +265,14 @@ SplitPlan split_plan(int num_kblocks, int requested) {
 constexpr double kUnitOverheadBlocks = 2.0;
 constexpr int kMaxGroupCounts = 32;
 constexpr long long kNoSearchRounds = 4 * kSchedEntries;  // zigzag's last round then costs < 0.5%
+constexpr int kPairTailMinBlocks = 24;
 
 int grid_for(const FwdParams& p, int num_sms) {
+  // pair tail: CTA pairs, twice the units when they all fit in one split round
+  if (p.pair_tail) {
+    const long long g = 2ll * p.num_units < num_sms ? 2ll * p.num_units : num_sms;
+    return static_cast<int>(g & ~1ll);
+  }
   // work items dealt to CTAs: units, or combined heavy+light pairs under zigzag
   const int items = p.order == kOrderZigzag ? p.BH * ((p.num_pairs + 1) / 2) : p.num_units;
   return items < num_sms ? items : num_sms;
@@ -282,7 +291,7 @@ double predicted_makespan(const FwdParams& p, int num_sms, int* max_rounds = nul
       const int u = unit_for_round(round, p, G, c);
       if (u == kNoMoreUnits) break;
       if (u == kSkipRound) continue;
-      const UnitInfo ui = unit_info(u, p);
+      const UnitInfo ui = unit_info(u, p, tail_role(round, p, G, c));
       t += (ui.n[1] > ui.n[0] ? ui.n[1] : ui.n[0]) + kUnitOverheadBlocks;
     }
     if (t > worst) worst = t;
@@ -299,6 +308,7 @@ struct OrderChoice {
 std::map<OrderKey, OrderChoice> g_order_cache;
 std::mutex g_order_mu;
 int g_force_order = -1, g_force_group_heads = 0;  // attn_diag_force_fwd_order
+std::atomic<bool> g_pair_tail_ok{true};            // attn_diag_set_pair_tail
 
 // table_cap: rounds the unit table of the launch's kTable instance holds (0: the
 // entry point has none)
@@ -311,6 +321,21 @@ void choose_order(FwdParams& p, int num_sms, long long kv_key_bytes, int table_c
     // head-major: ceil(units / grid) rounds
     const int G = grid_for(p, num_sms);
     p.sched_table = table_ok && (p.num_units + G - 1) / G <= table_cap ? 1 : 0;
+    // Pair tail (table launches, unsplit): when the last round holds at most one
+    // unit per CTA pair, each of its units is split over a pair, so that round
+    // takes half a unit's time (B1 H32 N4096: 512 units, 3.37 rounds of 152 CTAs
+    // -> 3.5 unit times instead of 4).  The cluster launch and the exchange cost
+    // ~12 us (measured: +4.7% at 32 key blocks of d = 128, -2% at 16), so only
+    // units of at least kPairTailMinBlocks key blocks (twice that at d = 64, whose
+    // blocks take about half the time) are split.
+    const int min_kb = kv_key_bytes >= 4 * 128 ? kPairTailMinBlocks : 2 * kPairTailMinBlocks;
+    if (p.sched_table && p.num_splits == 1 && p.num_kblocks >= min_kb && g_pair_tail_ok && num_sms >= 2) {
+      FwdParams c = p;
+      c.pair_tail = 1;
+      const int Gp = grid_for(c, num_sms);
+      const int full = p.num_units / Gp, rem = p.num_units - full * Gp;
+      if (rem > 0 && 2 * rem <= Gp && full + 1 <= table_cap) p.pair_tail = 1;
+    }
     return;
   }
   int force_order, force_hg;
@@ -409,14 +434,33 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
 
 // mo: tensor map of the bf16 output O (read only by the kTmaO instances)
 template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false,
-          bool kTable = false>
+          bool kTable = false, bool kPairTail = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
            const FwdParams& p, int dev, void* stream) {
-  if (static_cast<bool>(p.sched_table) != kTable) return ATTN_ERR_LAUNCH;  // the host's own bookkeeping
+  // the host's own bookkeeping: the instance matches the schedule
+  if (static_cast<bool>(p.sched_table) != kTable || static_cast<bool>(p.pair_tail) != kPairTail)
+    return ATTN_ERR_LAUNCH;
   const int grid = grid_for(p, g_dev[dev].num_sms);
-  attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO, kTable>
-      <<<grid, kNumThreads, SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>::kBytes,
-         static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mo, p);
+  constexpr size_t smem = SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>::kBytes;
+  auto kernel = attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO, kTable, kPairTail>;
+  if constexpr (kPairTail) {
+    // clusters of two CTAs (the pairs of the split last round)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, p) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  } else {
+    kernel<<<grid, kNumThreads, smem, static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mo, p);
+  }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -447,6 +491,10 @@ int launch_bf16(const void* q, const void* k, const void* v, int d, bool partial
   }
   CUtensorMap mo;
   if ((rc = make_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, p.Nq, p.BH, 64)) != ATTN_OK) return rc;
+  if (p.pair_tail) {
+    if (d == 64) return launch<ATTN_BF16_D64, false, false, true, true, true>(mq, mk, mv, mo, p, dev, stream);
+    return launch<ATTN_BF16_D128, false, false, true, true, true>(mq, mk, mv, mo, p, dev, stream);
+  }
   if (p.sched_table) {
     if (d == 64) return launch<ATTN_BF16_D64, false, false, true, true>(mq, mk, mv, mo, p, dev, stream);
     return launch<ATTN_BF16_D128, false, false, true, true>(mq, mk, mv, mo, p, dev, stream);
@@ -843,6 +891,11 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns, int* err) {
 }
 }  // namespace
 
+extern "C" int attn_diag_set_pair_tail(int enable) {
+  g_pair_tail_ok = enable != 0;
+  return ATTN_OK;
+}
+
 extern "C" int attn_diag_force_fwd_order(int order, int group_heads) {
   if (order < -1 || order > kOrderGroups || group_heads < 0) return ATTN_ERR_DIMS;
   std::lock_guard<std::mutex> lk(g_order_mu);
@@ -873,6 +926,7 @@ extern "C" int attn_diag_fwd_schedule(int BH, int Nq, int Nk, int causal, int q_
   info[3] = rounds;
   info[4] = static_cast<int>(std::llround(predicted_makespan(p, num_sms)));
   info[5] = p.sched_table;
+  info[6] = p.pair_tail;
   if (seq) {
     if (seq_len < static_cast<long long>(G) * rounds) return ATTN_ERR_WORKSPACE;
     for (int c = 0; c < G; ++c) {
@@ -880,7 +934,8 @@ extern "C" int attn_diag_fwd_schedule(int BH, int Nq, int Nk, int causal, int q_
       for (int r = 0; r < rounds; ++r) {
         const int u = done ? kNoMoreUnits : unit_for_round(r, p, G, c);
         done = done || u == kNoMoreUnits;
-        seq[static_cast<long long>(c) * rounds + r] = u;
+        // the second half of a pair-tail unit (the sending CTA) as -3 - u
+        seq[static_cast<long long>(c) * rounds + r] = (u >= 0 && tail_role(r, p, G, c) == 2) ? -3 - u : u;
       }
     }
   }

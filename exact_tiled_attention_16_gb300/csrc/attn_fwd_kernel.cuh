@@ -149,6 +149,8 @@ struct FwdParams {
   int order;          // unit order: kOrderHeads, kOrderZigzag or kOrderGroups (below)
   int group_heads;    // kOrderGroups: heads per group
   int sched_table;    // launched as a kTable instance (host bookkeeping)
+  int pair_tail;      // head-major, unsplit: the last, partly filled round's units are
+                      //   split in two key halves over the two CTAs of a cluster pair
   float scale_log2;   // scale * log2(e)
   const float* q_scale;  // FP8 only: [B*H, num_kblocks] block scales
   const float* k_scale;
@@ -173,7 +175,7 @@ struct TileLayout {
 // One round of a CTA's schedule, decoded (the unit table in shared memory).
 struct SchedEntry {
   int u;  // unit id, or kNoMoreUnits / kSkipRound
-  int bh, pair, split, kb0, n0, n1, pad;
+  int bh, pair, split, kb0, n0, n1, role;
 };
 constexpr int kSchedEntries = 64;     // rounds a CTA of a kTable instance may take
 constexpr int kSchedEntriesTma = 48;  // ... of a kTable instance with the O staging buffers
@@ -199,7 +201,7 @@ struct SmemPlan {
   static constexpr int kSchedN = kTable ? (kTmaO ? kSchedEntriesTma : kSchedEntries) : 0;
   static constexpr uint32_t kSched = kOst + (kTmaO ? kTilesPerUnit * kOstChunkBytes : 0);
   static constexpr uint32_t kBars = kSched + kSchedN * sizeof(SchedEntry);
-  static constexpr int kNumBars = 18 + 2 * NK + 2 * NV + 2 * kNumConv;
+  static constexpr int kNumBars = 21 + 2 * NK + 2 * NV + 2 * kNumConv;
   static constexpr size_t kBytes = 1024 /*alignment slack*/ + kBars + 8 * kNumBars + 16;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
@@ -225,9 +227,10 @@ struct UnitInfo {
   int bh, pair, split;
   int kb0;   // first K/V block of the unit's key range
   int n[2];  // K/V blocks tile 0 / tile 1 visit (n[1] >= n[0])
+  int role;  // pair tail: 0 a whole unit, 1 the first key half (merges), 2 the second (sends)
 };
 
-__host__ __device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p) {
+__host__ __device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p, int role = 0) {
   UnitInfo ui;
   const int per_head = p.num_pairs * p.num_splits;
   ui.bh = u / per_head;
@@ -235,9 +238,15 @@ __host__ __device__ __forceinline__ UnitInfo unit_info(int u, const FwdParams& p
   const int pr = r / p.num_splits;
   ui.split = r - pr * p.num_splits;
   ui.pair = p.causal ? (p.num_pairs - 1 - pr) : pr;
+  ui.role = role;
   ui.kb0 = ui.split * p.blocks_per_split;
   int kb_end = ui.kb0 + p.blocks_per_split;
   if (kb_end > p.num_kblocks) kb_end = p.num_kblocks;
+  if (role != 0) {  // pair tail (one split): the first or the second half of the key blocks
+    const int h = (p.num_kblocks + 1) / 2;
+    ui.kb0 = role == 1 ? 0 : h;
+    kb_end = role == 1 ? h : p.num_kblocks;
+  }
   for (int t = 0; t < kTilesPerUnit; ++t) {
     int hi = kb_end;
     if (p.causal) {
@@ -315,8 +324,25 @@ __host__ __device__ __forceinline__ int unit_for_round(int round, const FwdParam
     const int bh = g * hg + (q - pr * heads);
     return bh * p.num_pairs + pr;
   }
+  if (p.pair_tail) {
+    // full rounds as below; then unit full G + k for the CTA pair (2k, 2k+1)
+    const int full = p.num_units / G;
+    if (round > full) return kNoMoreUnits;
+    if (round == full) {
+      const int pos = full * G + (c >> 1);
+      return pos < p.num_units ? pos : kNoMoreUnits;
+    }
+  }
   const int pos = round * G + ((round & 1) ? (G - 1 - c) : c);
   return pos < p.num_units ? pos : kNoMoreUnits;
+}
+
+// The pair-tail role of CTA c in `round` (UnitInfo::role): 1 or 2 in the last
+// round of a pair-tail launch (the even CTA of the pair takes the first key half
+// and merges, the odd one the second half and sends), else 0.
+__host__ __device__ __forceinline__ int tail_role(int round, const FwdParams& p, int G, int c) {
+  if (!p.pair_tail || p.order != kOrderHeads || round != p.num_units / G) return 0;
+  return (p.num_units / G) * G + (c >> 1) < p.num_units ? 1 + (c & 1) : 0;
 }
 
 // The unit of the CTA's `round`-th iteration and its decoded info.  kTable
@@ -337,6 +363,7 @@ __device__ __forceinline__ int next_unit(int round, const SchedEntry* tab, const
     ui.kb0 = e.kb0;
     ui.n[0] = e.n0;
     ui.n[1] = e.n1;
+    ui.role = e.role;
     return e.u;
   } else {
     const int u = unit_for_round<false>(round, p, gridDim.x, blockIdx.x);
@@ -365,6 +392,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   const bool ok = mbar_wait(bar, parity, abort_flag, timeout_ns, err_word, where);
   return __all_sync(0xffffffffu, ok);
 }
+// The same for a barrier the partner CTA of a cluster pair arrives on.
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t timeout_ns, int* err_word, int where) {
+  const bool ok = mbar_wait_cluster(bar, parity, abort_flag, timeout_ns, err_word, where);
+  return __all_sync(0xffffffffu, ok);
+}
 
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
@@ -381,7 +414,7 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // only): O leaves through shared-memory staging and TMA stores instead of
 // row-per-thread global stores.
 template <int D, int NK, int NV, bool kFp8, bool kPartial, bool kFp4 = false, bool kTmaO = false,
-          bool kTable = false>
+          bool kTable = false, bool kPairTail = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
@@ -389,6 +422,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   static_assert(!kFp4 || (kFp8 && D == 128 && !kPartial), "Direct-P FP4: e4m3 Q K^T, d = 128, final output");
   static_assert(!kTmaO || !kPartial, "the TMA store serves the final bf16 output");
   using Plan = SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>;
+  static_assert(!kPairTail || (kTable && !kPartial && !kFp8), "the pair tail serves BF16 table launches");
   using L = typename Plan::In;
   using LV = typename Plan::V16;
   constexpr uint32_t kTmemS[2] = {0, 128};
@@ -422,6 +456,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const uint32_t b_pa_full = b_c_empty + 8 * Plan::kNumConv;  // + 8 t: first half of P_t written
   const uint32_t b_ost_ready = b_pa_full + 8 * kTilesPerUnit;   // + 8 t: staging chunk of tile t written
   const uint32_t b_ost_free = b_ost_ready + 8 * kTilesPerUnit;  // + 8 t: ... read by its TMA store
+  // pair tail: (+ 8 t) the partner's rows of tile t are in this CTA's shared memory;
+  // the partner's shared memory is free for this CTA's rows
+  const uint32_t b_data_ready = b_ost_free + 8 * kTilesPerUnit;
+  const uint32_t b_recv_ready = b_data_ready + 8 * kTilesPerUnit;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[Plan::kNumBars]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -441,6 +479,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       mbar_init(b_pa_full + 8 * t, 128);
       mbar_init(b_ost_ready + 8 * t, 128);
       mbar_init(b_ost_free + 8 * t, 1);
+      mbar_init(b_data_ready + 8 * t, 128);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(b_k_full + 8 * s, 1);
@@ -454,6 +493,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       mbar_init(b_c_full + 8 * b, kConvertThreads);
       mbar_init(b_c_empty + 8 * b, 1);
     }
+    mbar_init(b_recv_ready, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -471,8 +511,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   for (int i = threadIdx.x; i < Plan::kSchedN; i += kNumThreads) {
     SchedEntry e{};
     e.u = unit_for_round(i, p, gridDim.x, blockIdx.x);
+    e.role = tail_role(i, p, gridDim.x, blockIdx.x);
     if (e.u >= 0) {
-      const UnitInfo ui = unit_info(e.u, p);
+      const UnitInfo ui = unit_info(e.u, p, e.role);
       e.bh = ui.bh;
       e.pair = ui.pair;
       e.split = ui.split;
@@ -484,6 +525,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   }
   tc_fence_before();
   __syncthreads();
+  // pair tail: the partner's barriers are initialised before anyone arrives on them
+  if constexpr (kPairTail) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -607,11 +650,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
       };
       int o_uses[2] = {0, 0};  // units in which tile t has written O_t
+      bool merges = false;     // pair tail: this CTA receives its partner's half
       for (int round = 0; ok; ++round) {
         UnitInfo ui;
         const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
         if (u == kNoMoreUnits) break;
         if (u == kSkipRound) continue;
+        merges = merges || ui.role == 1;
         const int n0 = ui.n[0], n1 = ui.n[1];
         if (n1 == 0) continue;
         if (!(ok = warp_wait(b_q_full, units & 1, abort_flag, tmo, p.err, 10))) break;
@@ -694,7 +739,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       // Every MMA issued has completed before TMEM is released.
       mma_commit(b_drain);
       volatile int no_abort = 0;
-      warp_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
+      const bool drained = warp_wait(b_drain, 0, &no_abort, tmo, nullptr, 0);
+      if constexpr (kPairTail) {
+        // The CTA's last unit was its pair-tail half: no MMA reads and no TMA load
+        // writes the Q, K and V regions any more, so the partner may write its rows
+        // there (the softmax warps only read them after the partner's arrival).
+        if (merges && drained && (threadIdx.x & 31) == 0)
+          mbar_arrive_cluster(mapa_shared(b_recv_ready, cluster_ctarank() ^ 1u));
+        __syncwarp();
+      }
     } else if (Plan::kNumConv > 0 && warp >= kConvertWarp0) {
       // ------------------------------------------------- FP8: V e4m3 -> f16
       // Each thread converts 16 of the 1024 16-byte units of a V block (128 key
@@ -752,6 +805,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const uint32_t tO = tmem + lane_addr + kTmemO[t];
     uint32_t s_iter = 0, pv_iter = 0;
     uint32_t ost_uses = 0;  // TMA stores of O issued from this tile's staging chunk
+    int tail_role = 0, tail_bh = 0, tail_row = 0;  // pair tail: this CTA's split half
+    float tail_m = 0.f, tail_l = 0.f;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       UnitInfo ui;
@@ -975,6 +1030,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         if (!(ok = warp_wait(b_pv_done + 8 * t, pv_iter & 1, abort_flag, tmo, p.err, 22 + t))) break;
         ++pv_iter;
         tc_fence_after();
+        if constexpr (kPairTail) {
+          // the pair-tail half is always the CTA's last unit: its epilogue follows
+          // the loop.  The role is read again from the table here (a volatile
+          // load), so that no register carries it through the block loop.
+          const int role = reinterpret_cast<volatile const SchedEntry*>(sched)[round].role;
+          if (role != 0) {
+            tail_role = role;
+            tail_bh = bh;
+            tail_row = row;
+            tail_m = m_use;
+            tail_l = l;
+            break;
+          }
+        }
         const float inv_l = ((kFp8 && !kFp4) ? sv_max * (1.f / 64.f) : 1.f) / l;
         // O in 64-column chunks: each thread writes its row's 128 bytes of bf16
         // into the tile's staging chunk (the 128-byte swizzle the tensor map
@@ -1078,6 +1147,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
       }
     }
+    if constexpr (kPairTail) {
+      if (ok && tail_role != 0) {
+        // Pair tail: the odd CTA sends its half (O_t unnormalised, m, l per row)
+        // into the even CTA's Q/K/V regions; the even CTA merges the two halves
+        // the way split-K/V partials merge, normalises and stores.  Row layout:
+        // [m, l, 0, 0, O_0 .. O_{D-1}] in fp32, a 16-byte-aligned pitch whose
+        // 16-byte units fall in different bank groups for 8 consecutive rows.
+        // O_t moves 32 columns at a time (few live registers).
+        constexpr uint32_t kRowBytes = (D + 4) * 4;
+        static_assert(2 * kBlockM * kRowBytes <= Plan::kC, "pair-tail rows exceed the Q, K and V regions");
+        const uint32_t my_row = base + Plan::kQ + (t * kBlockM + row_in_tile) * kRowBytes;
+        const uint32_t peer = cluster_ctarank() ^ 1u;
+        if (tail_role == 2) {
+          if (warp_wait_cluster(b_recv_ready, 0, abort_flag, tmo, p.err, 32)) {
+            const uint32_t dst = mapa_shared(my_row, peer);
+            st_cluster_v4(dst, tail_m, tail_l, 0.f, 0.f);
+            for (int h = 0; h < D / 32; ++h) {
+              uint32_t oraw[32];
+              tmem_ld32_wait(tO + 32 * h, oraw);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                st_cluster_v4(dst + 16 + (32 * h + 4 * v) * 4, __uint_as_float(oraw[4 * v]),
+                              __uint_as_float(oraw[4 * v + 1]), __uint_as_float(oraw[4 * v + 2]),
+                              __uint_as_float(oraw[4 * v + 3]));
+            }
+            mbar_arrive_cluster(mapa_shared(b_data_ready + 8 * t, peer));
+          }
+        } else if (warp_wait_cluster(b_data_ready + 8 * t, 0, abort_flag, tmo, p.err, 33 + t)) {
+          const float4 ml = ld_shared_v4f(my_row);
+          const float m = fmaxf(tail_m, ml.x);
+          const float a0 = tail_m == -INFINITY ? 0.f : ex2_approx(tail_m - m);
+          const float a1 = ml.x == -INFINITY ? 0.f : ex2_approx(ml.x - m);
+          const float lt = tail_l * a0 + ml.y * a1;
+          const float w0 = a0 / lt, w1 = a1 / lt;
+          uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(tail_bh) * p.Nq + tail_row) * D);
+          for (int h = 0; h < D / 32; ++h) {
+            uint32_t oraw[32];
+            tmem_ld32_wait(tO + 32 * h, oraw);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const float4 x0 = ld_shared_v4f(my_row + 16 + (32 * h + 8 * v) * 4);
+              const float4 x1 = ld_shared_v4f(my_row + 16 + (32 * h + 8 * v + 4) * 4);
+              const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * w0 + xs[2 * e] * w1,
+                                   __uint_as_float(oraw[8 * v + 2 * e + 1]) * w0 + xs[2 * e + 1] * w1);
+              if (tail_row < p.Nq) dst[4 * h + v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          if (tail_row < p.Nq && p.lse != nullptr)
+            p.lse[static_cast<size_t>(tail_bh) * p.Nq + tail_row] = (m + lg2_approx(lt)) * 0.69314718055994530942f;
+        }
+      }
+    }
     // the TMA stores of O have completed before the CTA exits
     if constexpr (kTmaO) {
       if ((threadIdx.x & 127) == 0) bulk_wait_all();
@@ -1086,6 +1211,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
   tc_fence_before();
   __syncthreads();
+  // pair tail: neither CTA of a pair leaves while the other may still reach its
+  // shared memory (every wait above is bounded, so both get here)
+  if constexpr (kPairTail) cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

@@ -195,7 +195,11 @@ size_t attn_splitkv_static_scratch_bytes(void);
  * for full speed).  The B*H heads go through the device in up to eight chunks of
  * whole heads; the host->device copies of one chunk, the kernel of another and
  * the device->host copies of a third run on separate streams, so the transfers
- * overlap the computation.  Outputs are bitwise those of attn_fwd.
+ * overlap the computation.  Outputs equal those of attn_fwd up to rounding:
+ * each chunk is its own launch, and a non-causal launch whose last round is split
+ * over CTA pairs (attn_diag_fwd_schedule) merges two key halves of those rows, a
+ * different summation order; with the split off (attn_diag_set_pair_tail(0))
+ * they are bit for bit those of attn_fwd.
  *   workspace : device scratch of at least attn_fwd_host_workspace_bytes(B,H,N,d)
  *               bytes (else ATTN_ERR_WORKSPACE), 256-byte aligned, owned by the
  *               caller; the call overwrites it
@@ -331,13 +335,16 @@ int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, float* 
  * A unit is a pair of 128-row query tiles of one head: id = head * P + r with
  * P = ceil(Nq / 256) pairs per head; under the causal mask r = 0 is the heaviest
  * pair (the last rows), otherwise the first.
- * info (host, 6 ints): [0] order (0 head-major, 1 zigzag, 2 head groups), [1]
+ * info (host, 7 ints): [0] order (0 head-major, 1 zigzag, 2 head groups), [1]
  * heads per group, [2] CTAs launched, [3] rounds: the most iterations a CTA
  * takes, [4] the predicted time of the busiest CTA in K/V block periods, [5] 1
- * if the launch takes its units from the table.
+ * if the launch takes its units from the table, [6] 1 if the launch splits its
+ * last, partly filled round over CTA pairs (clusters of two: the even CTA takes
+ * the first half of the unit's key blocks and merges, the odd one the second).
  * seq (host, may be NULL): CTAs x rounds ints, seq[c * rounds + r] = the unit CTA
- * c takes in its r-th iteration, -2 for an iteration it skips, -1 once it is
- * done; seq_len: its capacity in ints (else ATTN_ERR_WORKSPACE).
+ * c takes in its r-th iteration (-3 - unit for the odd CTA of a split unit), -2
+ * for an iteration it skips, -1 once it is done; seq_len: its capacity in ints
+ * (else ATTN_ERR_WORKSPACE).
  * Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_DIMS, ATTN_ERR_OVERFLOW or
  * ATTN_ERR_WORKSPACE.
  */
@@ -355,6 +362,14 @@ int attn_diag_fwd_schedule(int BH, int Nq, int Nk, int causal, int q_offset, int
  * Returns ATTN_OK or ATTN_ERR_DIMS.
  */
 int attn_diag_force_fwd_order(int order, int group_heads);
+
+/*
+ * attn_diag_set_pair_tail -- diagnostics (no counterpart on the pages): enable
+ * (1, the default) or disable (0) the split of a launch's last, partly filled
+ * round over CTA pairs (see attn_diag_fwd_schedule) for every later launch of
+ * this process.  For tests and measurements that compare both.  Returns ATTN_OK.
+ */
+int attn_diag_set_pair_tail(int enable);
 
 #ifdef __cplusplus
 }

@@ -82,10 +82,18 @@ def test_deterministic_bitwise():
 
 
 def test_causal_last_row_equals_noncausal():
+    """The last causal row sees every key: bit for bit the non-causal row, both
+    computed in one pass over the keys (the non-causal launch's split of its last
+    round over CTA pairs, which merges two halves, is turned off here)."""
+    import exact_tiled_attention_16_gb300 as pkg
     wc = synth.make_bf16(1, 4, 1024, 128, True, seed=31)
     wn = synth.make_bf16(1, 4, 1024, 128, False, seed=31)
     oc, lc = run_bf16(wc)
-    on, ln_ = run_bf16(wn)
+    pkg.diag_set_pair_tail(False)
+    try:
+        on, ln_ = run_bf16(wn)
+    finally:
+        pkg.diag_set_pair_tail(True)
     np.testing.assert_array_equal(oc[:, :, -1], on[:, :, -1])
     np.testing.assert_array_equal(lc[:, :, -1], ln_[:, :, -1])
     # causal row 0 is v0 (rounded to bf16 twice at most)
@@ -242,6 +250,63 @@ def test_instances_past_the_unit_table(causal):
     o, lse = run_bf16(w)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     assert_bf16_tol(compare_rows(w, o, lse, rows_per_head=8), f"untabled causal={causal}")
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 4096, 128), (1, 3, 3100, 128), (1, 3, 6200, 64), (1, 2, 8192, 64),
+                                   (1, 32, 4096, 128)],
+                         ids=["all_split_d128", "ragged_odd_blocks_d128", "ragged_odd_blocks_d64", "all_split_d64",
+                              "B1H32N4096_tail_of_56"])
+def test_pair_tail_split_last_round(shape):
+    """Non-causal launches whose last round is split over CTA pairs (clusters of
+    two: the odd CTA sends its half's unnormalised O, max and sum through
+    distributed shared memory, the even CTA merges): rows against the oracle
+    (every row of the small cases, the split units' heads sampled in the large
+    one), and the result against the same launch with the split turned off."""
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    info, _ = pkg.diag_fwd_schedule(B * H, N, N, False, d=d, num_sms=sms)
+    if not info["pair_tail"]:
+        pytest.skip(f"{sms} SMs: this shape's last round is not split")
+    w = synth.make_bf16(B, H, N, d, False, seed=8800 + N + H)
+    o, lse = run_bf16(w)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    rows = None if B * H * N <= 20000 else 128
+    assert_bf16_tol(compare_rows(w, o, lse, rows_per_head=rows), f"pair tail {shape}")
+    pkg.diag_set_pair_tail(False)
+    try:
+        o2, lse2 = run_bf16(w)
+    finally:
+        pkg.diag_set_pair_tail(True)
+    assert np.abs(o - o2).max() <= 2e-2 and np.abs(lse - lse2).max() <= 1e-3
+
+
+@pytest.mark.parametrize("d,N", [(128, 3100), (64, 6200)])
+def test_pair_tail_writes_nothing_outside_outputs(d, N):
+    """The merging CTA of a split unit stores its rows directly: O and LSE inside
+    guard regions that must stay intact (ragged N, every unit split)."""
+    import exact_tiled_attention_16_gb300 as pkg
+    import exact_tiled_attention_16_gb300._lib as L
+    B, H = 1, 2
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if not pkg.diag_fwd_schedule(B * H, N, N, False, d=d, num_sms=sms)[0]["pair_tail"]:
+        pytest.skip("no pair tail on this device")
+    w = synth.make_bf16(B, H, N, d, False, seed=62)
+    q, k, v = to_device(w)
+    guard = 4096
+    o_buf = torch.full((B * H * N * d + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * N + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+    o_view = o_buf[guard:guard + B * H * N * d]
+    l_view = l_buf[guard:guard + B * H * N]
+    rc = L.attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_view.data_ptr(), l_view.data_ptr(),
+                        B, H, N, d, False, w.scale, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.isnan(o_buf[:guard].float()).all() and torch.isnan(o_buf[-guard:].float()).all()
+    assert torch.isnan(l_buf[:guard]).all() and torch.isnan(l_buf[-guard:]).all()
+    assert not torch.isnan(o_view.float()).any() and not torch.isnan(l_view).any()
+    assert_bf16_tol(compare_rows(w, o_view.view(B, H, N, d).float().cpu().numpy().astype(np.float64),
+                                 l_view.view(B, H, N).cpu().numpy().astype(np.float64)), "guarded pair tail")
 
 
 def _sweep_shapes():

@@ -117,8 +117,70 @@ def test_table_rule():
     assert info["order"] == GROUPS and info["table"] == 0
 
 
+def _noncausal_blocks(N, role):
+    nb = (N + 127) // 128
+    h = (nb + 1) // 2
+    return nb if role == 0 else (h if role == 1 else nb - h)
+
+
+@pytest.mark.parametrize("shape", [(32, 4096), (32, 16384), (2, 4096), (5, 3200), (64, 3000), (3, 6200)])
+def test_pair_tail_schedule(shape):
+    """Non-causal launches whose last round holds at most one unit per CTA pair
+    split each of its units over a pair (clusters of two): the even CTA takes the
+    first half of the key blocks (and merges), the odd one the second half,
+    encoded as -3 - unit.  Every unit is still dealt exactly once to an even CTA
+    or a whole-unit CTA, and the predicted makespan counts the halves."""
+    BH, N = shape
+    P = (N + 255) // 256
+    U = BH * P
+    info, seq = pkg.diag_fwd_schedule(BH, N, N, False)
+    G = info["grid"]
+    full, rem = divmod(U, G)
+    assert info["pair_tail"] == 1 and G % 2 == 0
+    assert 0 < rem <= G // 2
+    whole = seq[:, :full]
+    tail = seq[:, full] if seq.shape[1] > full else np.full(G, -1)
+    recv = tail[0::2]
+    send = tail[1::2]
+    assert np.array_equal(np.sort(np.concatenate([whole[whole >= 0], recv[recv >= 0]])), np.arange(U))
+    assert np.array_equal(recv[:rem], np.arange(full * G, U)) and (recv[rem:] == -1).all()
+    assert np.array_equal(send[:rem], -3 - recv[:rem]) and (send[rem:] == -1).all()
+    worst = 0.0
+    for c in range(G):
+        t = sum(_noncausal_blocks(N, 0) + 2.0 for u in seq[c, :full] if u >= 0)
+        if seq.shape[1] > full and seq[c, full] != -1:
+            t += _noncausal_blocks(N, 1 + (c & 1)) + 2.0
+        worst = max(worst, t)
+    assert info["makespan"] == round(worst)
+
+
+def test_pair_tail_only_when_the_last_round_fits_the_pairs():
+    # B1 H32 N8192: 1024 units = 6 rounds of 152 + 112 > 76 pairs: no pair tail
+    assert pkg.diag_fwd_schedule(32, 8192, 8192, False)[0]["pair_tail"] == 0
+    # too few key blocks for the split to pay (its fixed cost, measured): at least 24
+    # at d = 128, 48 at d = 64
+    assert pkg.diag_fwd_schedule(64, 2048, 2048, False)[0]["pair_tail"] == 0
+    assert pkg.diag_fwd_schedule(64, 3000, 3000, False)[0]["pair_tail"] == 1
+    assert pkg.diag_fwd_schedule(32, 4096, 4096, False, d=64)[0]["pair_tail"] == 0
+    assert pkg.diag_fwd_schedule(32, 16384, 16384, False, d=64)[0]["pair_tail"] == 1
+    # a single key block cannot be split; causal launches and other entry points keep whole units
+    assert pkg.diag_fwd_schedule(200, 128, 128, False)[0]["pair_tail"] == 0
+    assert pkg.diag_fwd_schedule(32, 4096, 4096, True)[0]["pair_tail"] == 0
+    assert pkg.diag_fwd_schedule(32, 4096, 4096, False, table_ok=False)[0]["pair_tail"] == 0
+    pkg.diag_set_pair_tail(False)
+    try:
+        assert pkg.diag_fwd_schedule(32, 4096, 4096, False)[0]["pair_tail"] == 0
+    finally:
+        pkg.diag_set_pair_tail(True)
+    assert pkg.diag_fwd_schedule(32, 4096, 4096, False)[0]["pair_tail"] == 1
+
+
 def test_noncausal_and_bad_arguments():
-    info, seq = pkg.diag_fwd_schedule(4, 1000, 1000, False)
+    pkg.diag_set_pair_tail(False)
+    try:
+        info, seq = pkg.diag_fwd_schedule(4, 1000, 1000, False)
+    finally:
+        pkg.diag_set_pair_tail(True)
     assert info["order"] == HEADS and info["table"] == 1
     # the non-causal table (beside the O staging buffers) holds 48 rounds
     assert pkg.diag_fwd_schedule(152 * 48, 256, 256, False)[0]["table"] == 1
