@@ -82,11 +82,13 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = False, table: bool = False) -> str:
+def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = False, table: bool = False,
+                    pair_tail: bool = False) -> str:
     """The forward kernel's template instance as ncu names it, read from the
     instance table of attn_api.cu (D, K stages, V stages, fp8, partial, fp4, the
-    TMA store of O, which the non-causal BF16 launches use, and the unit table,
-    which BF16 launches use when every CTA's rounds fit in it: `table`, from the
+    TMA store of O, which the non-causal BF16 launches use, the unit table, which
+    BF16 launches use when every CTA's rounds fit in it, and the pair tail, a
+    non-causal last round split over CTA pairs: `table` and `pair_tail` from the
     library's schedule diagnostic)."""
     import re
     text = open(os.path.join(CSRC, "attn_api.cu")).read()
@@ -98,8 +100,9 @@ def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = Fa
     fp4 = dtype == "e4m3_e2m1"
     tma_o = dtype == "bf16" and not partial and not causal
     tab = dtype == "bf16" and not partial and table
+    tail = tab and tma_o and pair_tail
     args = [D, nk, nv, "1" if fp8 == "true" else "0", "1" if partial else "0", "1" if fp4 else "0",
-            "1" if tma_o else "0", "1" if tab else "0"]
+            "1" if tma_o else "0", "1" if tab else "0", "1" if tail else "0"]
     return "attn::attn_fwd_kernel<" + ", ".join(args) + ">"
 
 
@@ -617,12 +620,12 @@ def main():
     elif decode:
         kname = kernel_instance(w.dtype, w.d, partial=True) + " + attn::attn_merge_kernel"
     else:
-        table = False
+        sched = {}
         if w.dtype == "bf16":
-            table = bool(pkg.diag_fwd_schedule(w.B * w.H, w.N, w.N, w.causal, d=w.d,
-                                               num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
-                         [0]["table"])
-        kname = kernel_instance(w.dtype, w.d, causal=w.causal, table=table)
+            sched = pkg.diag_fwd_schedule(w.B * w.H, w.N, w.N, w.causal, d=w.d,
+                                          num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)[0]
+        kname = kernel_instance(w.dtype, w.d, causal=w.causal, table=bool(sched.get("table")),
+                                pair_tail=bool(sched.get("pair_tail")))
     clocks = clk.summary()
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic_for(w.name + (":bwd" if bwd else "")), "peak_source": src,

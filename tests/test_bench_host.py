@@ -17,18 +17,23 @@ def test_kernel_instance_follows_the_instance_table():
     text = open(os.path.join(bench.CSRC, "attn_api.cu")).read()
     assert "#define ATTN_BF16_D128 128, 2, 2, false" in text
     # D, K stages, V stages, fp8, partial, fp4, TMA store of O (non-causal BF16 only),
-    # unit table (BF16 launches whose rounds fit in it)
-    assert bench.kernel_instance("bf16", 128, causal=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 0>"
+    # unit table (BF16 launches whose rounds fit in it), pair tail (non-causal table
+    # launches that split their last round over CTA pairs)
+    assert bench.kernel_instance("bf16", 128, causal=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 0, 0>"
     assert (bench.kernel_instance("bf16", 128, causal=True, table=True)
-            == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 1>")
-    assert bench.kernel_instance("bf16", 128, causal=False) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 1, 0>"
-    assert bench.kernel_instance("bf16", 64, causal=False) == "attn::attn_fwd_kernel<64, 4, 4, 0, 0, 0, 1, 0>"
+            == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 1, 0>")
+    assert bench.kernel_instance("bf16", 128, causal=False) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 1, 0, 0>"
+    assert bench.kernel_instance("bf16", 64, causal=False) == "attn::attn_fwd_kernel<64, 4, 4, 0, 0, 0, 1, 0, 0>"
     assert (bench.kernel_instance("bf16", 64, causal=False, table=True)
-            == "attn::attn_fwd_kernel<64, 4, 4, 0, 0, 0, 1, 1>")
-    assert bench.kernel_instance("bf16", 128, partial=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 1, 0, 0, 0>"
-    assert bench.kernel_instance("e4m3", 128) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0>"
-    assert bench.kernel_instance("e4m3_e2m1", 128) == "attn::attn_fwd_kernel<128, 4, 4, 1, 0, 1, 0, 0>"
-    assert bench.kernel_instance("e4m3", 128, causal=True, table=True) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0>"
+            == "attn::attn_fwd_kernel<64, 4, 4, 0, 0, 0, 1, 1, 0>")
+    assert (bench.kernel_instance("bf16", 128, causal=False, table=True, pair_tail=True)
+            == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 1, 1, 1>")
+    assert (bench.kernel_instance("bf16", 128, causal=True, table=True, pair_tail=True)
+            == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 1, 0>")
+    assert bench.kernel_instance("bf16", 128, partial=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 1, 0, 0, 0, 0>"
+    assert bench.kernel_instance("e4m3", 128) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0, 0>"
+    assert bench.kernel_instance("e4m3_e2m1", 128) == "attn::attn_fwd_kernel<128, 4, 4, 1, 0, 1, 0, 0, 0>"
+    assert bench.kernel_instance("e4m3", 128, causal=True, table=True) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0, 0>"
 
 
 def test_kernel_hash_covers_every_cuda_source(tmp_path, monkeypatch):
