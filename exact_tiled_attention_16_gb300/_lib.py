@@ -57,6 +57,11 @@ def load_library():
     lib.attn_fwd_host.restype = ci
     lib.attn_fwd_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
     lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_fwd_fp8_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, ctypes.c_size_t,
+                                      vp]
+    lib.attn_fwd_fp8_host.restype = ci
+    lib.attn_fwd_fp8_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.attn_fwd_fp8_host_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_fwd_fp4p.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
     lib.attn_fwd_fp4p.restype = ci
     lib.attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, vp]
@@ -184,6 +189,56 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sc
 
 def fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load_library().attn_fwd_host_workspace_bytes(B, H, N, d))
+
+
+def fp8_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().attn_fwd_fp8_host_workspace_bytes(B, H, N, d))
+
+
+def attn_fwd_fp8_host_raw(q8: int, k8: int, v8: int, q_scale: int, k_scale: int, v_scale: int, o: int, lse: int,
+                          B: int, H: int, N: int, d: int, causal: bool, scale: float, workspace: int,
+                          workspace_bytes: int, stream: int) -> int:
+    return load_library().attn_fwd_fp8_host(q8 or None, k8 or None, v8 or None, q_scale or None, k_scale or None,
+                                            v_scale or None, o or None, lse or None, B, H, N, d,
+                                            1 if causal else 0, float(scale), workspace or None,
+                                            int(workspace_bytes), stream or None)
+
+
+def attn_fwd_fp8_host(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, scale: float | None = None,
+                      o=None, lse=None, want_lse: bool = True, workspace=None, stream=None):
+    """attn_fwd_fp8 on HOST tensors (page-locked for full speed): e4m3 codes
+    q8, k8, v8 [B,H,N,d] (1-byte dtype) and float32 block scales [B,H,ceil(N/128)];
+    transfers and kernels are pipelined by the library.  Returns host (o bf16,
+    lse), valid once `stream` (default: torch's current stream) has completed.  The
+    device workspace is allocated with torch when not given."""
+    import torch
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if t.element_size() != 1 or t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous host e4m3 (1-byte) tensor [B,H,N,d]")
+    if k8.shape != q8.shape or v8.shape != q8.shape:
+        raise ValueError("q8, k8 and v8 must have the same shape [B,H,N,d]")
+    B, H, N, d = q8.shape
+    T = (N + 127) // 128
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        if t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, H, T):
+            raise ValueError(f"{name} must be a contiguous host float32 tensor [B,H,ceil(N/128)]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q8.is_pinned()
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    need = fp8_host_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = attn_fwd_fp8_host_raw(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
+                               v_scale.data_ptr(), o.data_ptr(), lse.data_ptr() if lse is not None else 0,
+                               B, H, N, d, causal, scale, workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8_host")
+    return o, lse
 
 
 def attn_fwd_host_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int, causal: bool,

@@ -192,21 +192,59 @@ int pipe_setup(HostPipe& hp) {
   return ATTN_OK;
 }
 
+// A tensor the pipeline moves: host buffer and bytes per head (whole heads are
+// contiguous in every layout the entry points take).
+struct HostTensor {
+  const void* in;  // host source (inputs), or null
+  void* out;       // host destination (outputs), or null
+  size_t per_head;
+};
+constexpr int kHostMaxTensors = 8;
+
 struct HostChunking {
   int heads;          // heads per chunk (the last chunk may hold fewer)
   int chunks;
-  size_t slot_bytes;  // Q, K, V and O of a chunk (bf16) and its LSE (fp32), 256-byte aligned
+  size_t region[kHostMaxTensors];  // bytes of each tensor's region in a slot (256-byte multiples)
+  size_t slot_bytes;  // all of a chunk's tensors
 };
-HostChunking host_chunking(int B, int H, int N, int d) {
+HostChunking host_chunking(int B, int H, const HostTensor* t, int nt) {
   HostChunking hc;
   const long long BH = static_cast<long long>(B) * H;
   const long long n = BH < kHostChunks ? BH : kHostChunks;
   hc.heads = static_cast<int>((BH + n - 1) / n);
   hc.chunks = static_cast<int>((BH + hc.heads - 1) / hc.heads);
-  const size_t t = static_cast<size_t>(hc.heads) * N * d * 2;  // one bf16 tensor of a chunk (multiple of 128)
-  const size_t l = (static_cast<size_t>(hc.heads) * N * sizeof(float) + 255) / 256 * 256;
-  hc.slot_bytes = 4 * t + l;
+  hc.slot_bytes = 0;
+  for (int i = 0; i < nt; ++i) {
+    hc.region[i] = (static_cast<size_t>(hc.heads) * t[i].per_head + 255) / 256 * 256;
+    hc.slot_bytes += hc.region[i];
+  }
   return hc;
+}
+// The BF16 path's tensors: Q, K, V in; O, LSE out.
+int bf16_host_tensors(HostTensor* t, const void* q, const void* k, const void* v, void* o, float* lse, int N,
+                      int d) {
+  const size_t hb = static_cast<size_t>(N) * d * 2;
+  t[0] = {q, nullptr, hb};
+  t[1] = {k, nullptr, hb};
+  t[2] = {v, nullptr, hb};
+  t[3] = {nullptr, o, hb};
+  t[4] = {nullptr, lse, static_cast<size_t>(N) * sizeof(float)};
+  return 5;
+}
+// The FP8 path's tensors: e4m3 Q, K, V and their block scales in; O, LSE out.
+int fp8_host_tensors(HostTensor* t, const void* q8, const void* k8, const void* v8, const float* qs,
+                     const float* ks, const float* vs, void* o, float* lse, int N, int d) {
+  const size_t hb = static_cast<size_t>(N) * d;
+  const size_t sb = static_cast<size_t>((N + kBlockN - 1) / kBlockN) * sizeof(float);
+  t[0] = {q8, nullptr, hb};
+  t[1] = {k8, nullptr, hb};
+  t[2] = {v8, nullptr, hb};
+  t[3] = {qs, nullptr, sb};
+  t[4] = {ks, nullptr, sb};
+  t[5] = {vs, nullptr, sb};
+  t[6] = {nullptr, o, 2 * hb};
+  t[7] = {nullptr, lse, static_cast<size_t>(N) * sizeof(float)};
+  return 8;
 }
 
 // Largest sequence length accepted: keeps every position and mask limit of the
@@ -555,6 +593,66 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   attn_bwd_dkdv_kernel<D, RA, RB><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
+// The pipeline of the host-buffer entry points: chunks of whole heads through two
+// workspace slots; per chunk the inputs are copied in on s_in, `launch(h0, hn,
+// dev)` runs the kernel on the caller's stream with dev[i] = the slot's region of
+// tensor i, and the outputs are copied back on s_out.  Null host pointers (an
+// optional LSE) are skipped.
+template <class Launch>
+int host_pipeline(const HostTensor* t, int nt, const HostChunking& hcfg, long long BH, void* workspace, int dev,
+                  void* stream, Launch launch) {
+  HostPipe& hp = g_pipe[dev];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  int rc;
+  if ((rc = pipe_setup(hp)) != ATTN_OK) return rc;
+  cudaStream_t sc = static_cast<cudaStream_t>(stream);
+  bool ok = true;
+  auto ck = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+  // the copies wait for earlier work on the caller's stream (it may still use the workspace)
+  ck(cudaEventRecord(hp.entry, sc));
+  ck(cudaStreamWaitEvent(hp.s_in, hp.entry, 0));
+  ck(cudaStreamWaitEvent(hp.s_out, hp.entry, 0));
+  for (int c = 0; c < hcfg.chunks && ok; ++c) {
+    const int slot = c % kHostSlots;
+    const long long h0 = static_cast<long long>(c) * hcfg.heads;
+    const int hn = static_cast<int>(BH - h0 < hcfg.heads ? BH - h0 : hcfg.heads);
+    uint8_t* reg[kHostMaxTensors];
+    uint8_t* base = static_cast<uint8_t*>(workspace) + slot * hcfg.slot_bytes;
+    for (int i = 0; i < nt; ++i) {
+      reg[i] = base;
+      base += hcfg.region[i];
+    }
+    // copy in, once the kernel two chunks back is done with this slot's inputs
+    if (c >= kHostSlots) ck(cudaStreamWaitEvent(hp.s_in, hp.comp_done[slot], 0));
+    for (int i = 0; i < nt; ++i)
+      if (t[i].in)
+        ck(cudaMemcpyAsync(reg[i], static_cast<const uint8_t*>(t[i].in) + h0 * t[i].per_head, hn * t[i].per_head,
+                           cudaMemcpyHostToDevice, hp.s_in));
+    ck(cudaEventRecord(hp.in_done[slot], hp.s_in));
+    // the kernel, once the inputs are in and the copy-out two chunks back has read the outputs
+    ck(cudaStreamWaitEvent(sc, hp.in_done[slot], 0));
+    if (c >= kHostSlots) ck(cudaStreamWaitEvent(sc, hp.out_done[slot], 0));
+    if (!ok) break;
+    if ((rc = launch(h0, hn, reg)) != ATTN_OK) return rc;
+    ck(cudaEventRecord(hp.comp_done[slot], sc));
+    // copy out
+    ck(cudaStreamWaitEvent(hp.s_out, hp.comp_done[slot], 0));
+    for (int i = 0; i < nt; ++i)
+      if (t[i].out)
+        ck(cudaMemcpyAsync(static_cast<uint8_t*>(t[i].out) + h0 * t[i].per_head, reg[i], hn * t[i].per_head,
+                           cudaMemcpyDeviceToHost, hp.s_out));
+    ck(cudaEventRecord(hp.out_done[slot], hp.s_out));
+  }
+  // work queued on the caller's stream after this call sees the outputs in host memory
+  ck(cudaEventRecord(hp.last, hp.s_out));
+  ck(cudaStreamWaitEvent(sc, hp.last, 0));
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int BH, int N, int d, int causal, float scale, int dev,
+               void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -576,7 +674,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
-  return kHostSlots * host_chunking(B, H, N, d).slot_bytes;
+  HostTensor t[kHostMaxTensors];
+  const int nt = bf16_host_tensors(t, nullptr, nullptr, nullptr, nullptr, nullptr, N, d);
+  return kHostSlots * host_chunking(B, H, t, nt).slot_bytes;
 }
 
 int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -585,60 +685,28 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
   if (rc != ATTN_OK) return rc;
   if (!workspace) return ATTN_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
-  const HostChunking hcfg = host_chunking(B, H, N, d);
+  HostTensor t[kHostMaxTensors];
+  const int nt = bf16_host_tensors(t, q, k, v, o, lse, N, d);
+  const HostChunking hcfg = host_chunking(B, H, t, nt);
   if (workspace_bytes < kHostSlots * hcfg.slot_bytes) return ATTN_ERR_WORKSPACE;
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
-  HostPipe& hp = g_pipe[dev];
-  std::lock_guard<std::mutex> lock(hp.mu);
-  if ((rc = pipe_setup(hp)) != ATTN_OK) return rc;
-  cudaStream_t sc = static_cast<cudaStream_t>(stream);
-  const long long BH = static_cast<long long>(B) * H;
-  const size_t head_bytes = static_cast<size_t>(N) * d * 2;
-  const size_t chunk_in = static_cast<size_t>(hcfg.heads) * head_bytes;
-  bool ok = true;
-  auto ck = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
-  // the copies wait for earlier work on the caller's stream (it may still use the workspace)
-  ck(cudaEventRecord(hp.entry, sc));
-  ck(cudaStreamWaitEvent(hp.s_in, hp.entry, 0));
-  ck(cudaStreamWaitEvent(hp.s_out, hp.entry, 0));
-  for (int c = 0; c < hcfg.chunks && ok; ++c) {
-    const int slot = c % kHostSlots;
-    const long long h0 = static_cast<long long>(c) * hcfg.heads;
-    const int hn = static_cast<int>(BH - h0 < hcfg.heads ? BH - h0 : hcfg.heads);
-    const size_t bytes = static_cast<size_t>(hn) * head_bytes;
-    uint8_t* base = static_cast<uint8_t*>(workspace) + slot * hcfg.slot_bytes;
-    uint8_t *dq = base, *dk = dq + chunk_in, *dv = dk + chunk_in, *dout = dv + chunk_in;
-    float* dl = reinterpret_cast<float*>(dout + chunk_in);
-    // copy in, once the kernel two chunks back is done with this slot's inputs
-    if (c >= kHostSlots) ck(cudaStreamWaitEvent(hp.s_in, hp.comp_done[slot], 0));
-    ck(cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + h0 * head_bytes, bytes, cudaMemcpyHostToDevice, hp.s_in));
-    ck(cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + h0 * head_bytes, bytes, cudaMemcpyHostToDevice, hp.s_in));
-    ck(cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + h0 * head_bytes, bytes, cudaMemcpyHostToDevice, hp.s_in));
-    ck(cudaEventRecord(hp.in_done[slot], hp.s_in));
-    // the kernel, once the inputs are in and the copy-out two chunks back has read the outputs
-    ck(cudaStreamWaitEvent(sc, hp.in_done[slot], 0));
-    if (c >= kHostSlots) ck(cudaStreamWaitEvent(sc, hp.out_done[slot], 0));
-    if (!ok) break;
-    FwdParams p;
-    fill_params(p, hn, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 4ll * d, true);
-    p.err = g_dev[dev].err_ptr;
-    p.o = reinterpret_cast<__nv_bfloat16*>(dout);
-    p.lse = lse ? dl : nullptr;
-    if ((rc = launch_bf16(dq, dk, dv, d, false, p, dev, sc)) != ATTN_OK) return rc;
-    ck(cudaEventRecord(hp.comp_done[slot], sc));
-    // copy out
-    ck(cudaStreamWaitEvent(hp.s_out, hp.comp_done[slot], 0));
-    ck(cudaMemcpyAsync(static_cast<uint8_t*>(o) + h0 * head_bytes, dout, bytes, cudaMemcpyDeviceToHost, hp.s_out));
-    if (lse)
-      ck(cudaMemcpyAsync(lse + h0 * N, dl, static_cast<size_t>(hn) * N * sizeof(float), cudaMemcpyDeviceToHost,
-                         hp.s_out));
-    ck(cudaEventRecord(hp.out_done[slot], hp.s_out));
-  }
-  // work queued on the caller's stream after this call sees the outputs in host memory
-  ck(cudaEventRecord(hp.last, hp.s_out));
-  ck(cudaStreamWaitEvent(sc, hp.last, 0));
-  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+  return host_pipeline(t, nt, hcfg, static_cast<long long>(B) * H, workspace, dev, stream,
+                       [&](long long, int hn, uint8_t* const* reg) {
+                         FwdParams p;
+                         fill_params(p, hn, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 4ll * d, true);
+                         p.err = g_dev[dev].err_ptr;
+                         p.o = reinterpret_cast<__nv_bfloat16*>(reg[3]);
+                         p.lse = lse ? reinterpret_cast<float*>(reg[4]) : nullptr;
+                         return launch_bf16(reg[0], reg[1], reg[2], d, false, p, dev, stream);
+                       });
+}
+
+size_t attn_fwd_fp8_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d != 128) return 0;
+  HostTensor t[kHostMaxTensors];
+  const int nt = fp8_host_tensors(t, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, N, d);
+  return kHostSlots * host_chunking(B, H, t, nt).slot_bytes;
 }
 
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
@@ -653,7 +721,41 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
     return ATTN_ERR_ALIGN;
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
-  const int BH = B * H;
+  return launch_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B * H, N, d, causal, scale, dev, stream);
+}
+
+int attn_fwd_fp8_host(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                      const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_tensors(q8, k8, v8, o, lse, B, H, N, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  if (!q_scale || !k_scale || !v_scale || !workspace) return ATTN_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
+  HostTensor t[kHostMaxTensors];
+  const int nt = fp8_host_tensors(t, q8, k8, v8, q_scale, k_scale, v_scale, o, lse, N, d);
+  const HostChunking hcfg = host_chunking(B, H, t, nt);
+  if (workspace_bytes < kHostSlots * hcfg.slot_bytes) return ATTN_ERR_WORKSPACE;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  return host_pipeline(t, nt, hcfg, static_cast<long long>(B) * H, workspace, dev, stream,
+                       [&](long long, int hn, uint8_t* const* reg) {
+                         return launch_fp8(reg[0], reg[1], reg[2], reinterpret_cast<const float*>(reg[3]),
+                                           reinterpret_cast<const float*>(reg[4]),
+                                           reinterpret_cast<const float*>(reg[5]), reg[6],
+                                           lse ? reinterpret_cast<float*>(reg[7]) : nullptr, hn, N, d, causal,
+                                           scale, dev, stream);
+                       });
+}
+
+}  // extern "C"
+
+namespace {
+// The FP8 forward over BH heads of device tensors (arguments already checked).
+int launch_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int BH, int N, int d, int causal, float scale, int dev,
+               void* stream) {
+  int rc;
   CUtensorMap mq, mk, mv;
   if ((rc = make_map(&mq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
@@ -668,6 +770,9 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
   p.v_scale = v_scale;
   return launch<ATTN_FP8_D128, false>(mq, mk, mv, mq, p, dev, stream);
 }
+}  // namespace
+
+extern "C" {
 
 int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* q_scale, const float* k_scale,
                   const uint8_t* vt_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,

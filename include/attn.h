@@ -215,6 +215,27 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
 size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * attn_fwd_fp8_host -- attn_fwd_fp8 with its inputs and outputs in HOST memory
+ * (page-locked for full speed): e4m3 Q, K, V [B,H,N,d] and their fp32 block scales
+ * [B,H,ceil(N/128)] in, O bf16 [B,H,N,d] and LSE fp32 [B,H,N] (may be NULL) out.
+ * The heads go through the device in up to eight chunks with the copies of one
+ * chunk and the kernel of another on separate streams, as attn_fwd_host; each
+ * chunk runs attn_fwd_fp8's kernel on whole heads, so the outputs are bit for
+ * bit those of attn_fwd_fp8.
+ *   workspace : device scratch of at least attn_fwd_fp8_host_workspace_bytes(B,H,N,d)
+ *               bytes (else ATTN_ERR_WORKSPACE), 256-byte aligned, owned by the
+ *               caller; the call overwrites it
+ *   stream    : as attn_fwd_host
+ * Returns the codes of attn_fwd_fp8 and attn_fwd_host.
+ */
+int attn_fwd_fp8_host(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                      const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device scratch attn_fwd_fp8_host needs (0 for invalid arguments). */
+size_t attn_fwd_fp8_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * attn_fwd_fp4p -- Direct-P FP4 forward (the "Hardware-Aware FP4
  * FlashAttention-4" summary: Direct-P for non-causal inference on Blackwell's
  * FP4 tensor cores).  Q K^T as in attn_fwd_fp8; P V on the FP4 tensor cores with

@@ -98,3 +98,46 @@ def test_workspace_too_small_launches_nothing():
     assert rc == L.ATTN_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert (o.float() == 7.0).all()
+
+
+FP8_SHAPES = [(1, 2, 1000, 128, False), (2, 9, 700, 128, True), (1, 32, 2048, 128, False)]
+
+
+@pytest.mark.parametrize("pin", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("shape", FP8_SHAPES, ids=[f"B{b}H{h}N{n}{'c' if c else 'n'}" for b, h, n, d, c in FP8_SHAPES])
+def test_fp8_host_bitwise_equal_to_device_call(shape, pin):
+    """attn_fwd_fp8_host: the e4m3 codes and block scales in host memory, pipelined
+    in chunks of whole heads; every chunk runs attn_fwd_fp8's kernel, which never
+    splits a unit, so the outputs are bit for bit those of attn_fwd_fp8."""
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d, causal = shape
+    w = synth.make_fp8(B, H, N, d, causal, seed=700 + N)
+
+    def host(x):
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        return t.pin_memory() if pin else t.clone()
+    q8, k8, v8, qs, ks, vs = (host(x) for x in (w.q, w.k, w.v, w.q_scale, w.k_scale, w.v_scale))
+    o_h, l_h = pkg.attn_fwd_fp8_host(q8, k8, v8, qs, ks, vs, causal=causal, scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    o_d, l_d = pkg.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qs.cuda(), ks.cuda(), vs.cuda(), causal=causal,
+                                scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h.view(torch.int16), o_d.cpu().view(torch.int16))
+    assert torch.equal(l_h.view(torch.int32), l_d.cpu().view(torch.int32))
+    assert pkg.check_device_errors()[0] == 0
+
+
+def test_fp8_host_workspace_too_small_launches_nothing():
+    import exact_tiled_attention_16_gb300._lib as L
+    B, H, N, d = 1, 2, 256, 128
+    q = torch.zeros(B, H, N, d, dtype=torch.uint8).pin_memory()
+    sc = torch.ones(B, H, N // 128, dtype=torch.float32).pin_memory()
+    o = torch.full((B, H, N, d), 7.0, dtype=torch.bfloat16).pin_memory()
+    need = L.fp8_host_workspace_bytes(B, H, N, d)
+    assert need > 0 and L.fp8_host_workspace_bytes(B, H, N, 64) == 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    rc = L.attn_fwd_fp8_host_raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), sc.data_ptr(), sc.data_ptr(), sc.data_ptr(),
+                                 o.data_ptr(), 0, B, H, N, d, False, 0.1, ws.data_ptr(), need - 256, 0)
+    assert rc == L.ATTN_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert (o.float() == 7.0).all()
