@@ -553,7 +553,7 @@ def main():
 
     # end to end through the public API: pinned host inputs -> device, the pass,
     # its results back to pinned host memory, every step.  Forward: Q, K, V in,
-    # O and LSE out (BF16: one attn_fwd_host call, FP8: one attn_fwd_fp8_host call,
+    # O and LSE out (one attn_fwd_host, attn_fwd_fp8_host or attn_fwd_fp4p_host call,
     # which pipeline the transfers with the kernels).  Backward: Q, K, V, O, dO, LSE
     # in, dQ, dK, dV out.
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
@@ -570,13 +570,18 @@ def main():
         in_host = [q_h, k_h, v_h] + list(sc_h)
     outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
 
-    # the BF16 and FP8 forwards: the library's pipelined host-buffer entry points
-    host_api = not (bwd or fp4 or decode)
+    # the BF16, FP8 and Direct-P FP4 forwards: the library's pipelined host-buffer entry points
+    host_api = not (bwd or decode)
     if host_api:
-        need = (pkg.fp8_host_workspace_bytes if fp8 else pkg.fwd_host_workspace_bytes)(w.B, w.H, Nq, w.d)
+        need = (pkg.fp4p_host_workspace_bytes if fp4 else pkg.fp8_host_workspace_bytes if fp8
+                else pkg.fwd_host_workspace_bytes)(w.B, w.H, Nq, w.d)
         hws = torch.empty(need, dtype=torch.uint8, device=dev)
 
     def e2e_step():
+        if host_api and fp4:
+            pkg.attn_fwd_fp4p_host(q_h, k_h, v_h, *sc_h, causal=w.causal, scale=w.scale, o=outs_h[0],
+                                   lse=outs_h[1], workspace=hws)
+            return
         if host_api and fp8:
             pkg.attn_fwd_fp8_host(q_h, k_h, v_h, *sc_h, causal=w.causal, scale=w.scale, o=outs_h[0],
                                   lse=outs_h[1], workspace=hws)
@@ -694,7 +699,7 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": int(sum(t.nbytes for t in in_host)),
                 "d2h_bytes_per_step": int(sum(t.nbytes for t in outs_h)),
-                "api": ((("attn_fwd_fp8_host" if fp8 else "attn_fwd_host")
+                "api": ((("attn_fwd_fp4p_host" if fp4 else "attn_fwd_fp8_host" if fp8 else "attn_fwd_host")
                          + ": pinned host buffers, chunked copies overlapped with the kernels")
                         if host_api else "pinned host copies in, the pass, copies out, on one stream")},
         "gpu_launches": args.steps * launches_per_step,

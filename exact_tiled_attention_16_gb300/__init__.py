@@ -9,7 +9,7 @@ functions load the library on first use and raise if it is missing.
 """
 from __future__ import annotations
 
-__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_fp8", "attn_fwd_fp8_raw", "attn_fwd_fp4p", "attn_fwd_fp4p_raw", "attn_fwd_host", "attn_fwd_host_raw", "fwd_host_workspace_bytes", "attn_fwd_fp8_host", "attn_fwd_fp8_host_raw", "fp8_host_workspace_bytes", "attn_status_string", "load_library", "AttnError",
+__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_fp8", "attn_fwd_fp8_raw", "attn_fwd_fp4p", "attn_fwd_fp4p_raw", "attn_fwd_host", "attn_fwd_host_raw", "fwd_host_workspace_bytes", "attn_fwd_fp8_host", "attn_fwd_fp8_host_raw", "fp8_host_workspace_bytes", "attn_fwd_fp4p_host", "attn_fwd_fp4p_host_raw", "fp4p_host_workspace_bytes", "attn_status_string", "load_library", "AttnError",
            "attn_fwd_partial", "attn_fwd_partial_raw", "attn_merge", "attn_merge_raw",
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
            "attn_bwd", "attn_bwd_raw", "bwd_workspace_bytes",

@@ -62,6 +62,11 @@ def load_library():
     lib.attn_fwd_fp8_host.restype = ci
     lib.attn_fwd_fp8_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
     lib.attn_fwd_fp8_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_fwd_fp4p_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp,
+                                       ctypes.c_size_t, vp]
+    lib.attn_fwd_fp4p_host.restype = ci
+    lib.attn_fwd_fp4p_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.attn_fwd_fp4p_host_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_fwd_fp4p.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
     lib.attn_fwd_fp4p.restype = ci
     lib.attn_fwd_partial.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, vp]
@@ -277,6 +282,53 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, o=N
                            _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_host")
+    return o, lse
+
+
+def fp4p_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().attn_fwd_fp4p_host_workspace_bytes(B, H, N, d))
+
+
+def attn_fwd_fp4p_host_raw(q8: int, k8: int, vt4: int, q_scale: int, k_scale: int, vt_scale: int, o: int, lse: int,
+                           B: int, H: int, N: int, d: int, causal: bool, scale: float, workspace: int,
+                           workspace_bytes: int, stream: int) -> int:
+    return load_library().attn_fwd_fp4p_host(q8 or None, k8 or None, vt4 or None, q_scale or None, k_scale or None,
+                                             vt_scale or None, o or None, lse or None, B, H, N, d,
+                                             1 if causal else 0, float(scale), workspace or None,
+                                             int(workspace_bytes), stream or None)
+
+
+def attn_fwd_fp4p_host(q8, k8, vt4, q_scale, k_scale, vt_scale, causal: bool = False, scale: float | None = None,
+                       o=None, lse=None, want_lse: bool = True, workspace=None, stream=None):
+    """attn_fwd_fp4p on HOST tensors (page-locked for full speed), in its layouts;
+    transfers and kernels are pipelined by the library.  Returns host (o bf16,
+    lse), valid once `stream` (default: torch's current stream) has completed."""
+    import torch
+    for name, t, dt in (("q8", q8, torch.uint8), ("k8", k8, torch.uint8), ("vt4", vt4, torch.uint8),
+                        ("q_scale", q_scale, torch.float32), ("k_scale", k_scale, torch.float32),
+                        ("vt_scale", vt_scale, torch.uint8)):
+        if t.dtype != dt or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host {dt} tensor")
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or vt4.shape != (B, H, d, N // 2) or vt_scale.shape != (B, H, d, N // 32):
+        raise ValueError("shapes: q8, k8 [B,H,N,d]; vt4 [B,H,d,N/2]; vt_scale [B,H,d,N/32]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q8.is_pinned()
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    need = fp4p_host_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = attn_fwd_fp4p_host_raw(q8.data_ptr(), k8.data_ptr(), vt4.data_ptr(), q_scale.data_ptr(),
+                                k_scale.data_ptr(), vt_scale.data_ptr(), o.data_ptr(),
+                                lse.data_ptr() if lse is not None else 0, B, H, N, d, causal, scale,
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp4p_host")
     return o, lse
 
 

@@ -246,6 +246,21 @@ int fp8_host_tensors(HostTensor* t, const void* q8, const void* k8, const void* 
   t[7] = {nullptr, lse, static_cast<size_t>(N) * sizeof(float)};
   return 8;
 }
+// The Direct-P FP4 path's tensors: e4m3 Q, K, e2m1 V^T, the Q and K block scales and
+// the E8M0 scales of V^T in; O, LSE out.
+int fp4p_host_tensors(HostTensor* t, const void* q8, const void* k8, const void* vt4, const float* qs,
+                      const float* ks, const uint8_t* vts, void* o, float* lse, int N, int d) {
+  const size_t hb = static_cast<size_t>(N) * d;
+  t[0] = {q8, nullptr, hb};
+  t[1] = {k8, nullptr, hb};
+  t[2] = {vt4, nullptr, hb / 2};
+  t[3] = {qs, nullptr, static_cast<size_t>(N / kBlockN) * sizeof(float)};
+  t[4] = {ks, nullptr, static_cast<size_t>(N / kBlockN) * sizeof(float)};
+  t[5] = {vts, nullptr, static_cast<size_t>(d) * (N / 32)};
+  t[6] = {nullptr, o, 2 * hb};
+  t[7] = {nullptr, lse, static_cast<size_t>(N) * sizeof(float)};
+  return 8;
+}
 
 // Largest sequence length accepted: keeps every position and mask limit of the
 // kernels inside 32-bit integers.
@@ -652,6 +667,9 @@ int host_pipeline(const HostTensor* t, int nt, const HostChunking& hcfg, long lo
 int launch_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
                const float* v_scale, void* o, float* lse, int BH, int N, int d, int causal, float scale, int dev,
                void* stream);
+int launch_fp4p(const void* q8, const void* k8, const void* vt4, const float* q_scale, const float* k_scale,
+                const uint8_t* vt_scale, void* o, float* lse, int BH, int N, int d, int causal, float scale, int dev,
+                void* stream);
 
 }  // namespace
 
@@ -789,7 +807,50 @@ int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* 
     return ATTN_ERR_ALIGN;
   int dev = 0;
   if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
-  const int BH = B * H;
+  return launch_fp4p(q8, k8, vt4, q_scale, k_scale, vt_scale, o, lse, B * H, N, d, causal, scale, dev, stream);
+}
+
+int attn_fwd_fp4p_host(const void* q8, const void* k8, const void* vt4, const float* q_scale, const float* k_scale,
+                       const uint8_t* vt_scale, void* o, float* lse, int B, int H, int N, int d, int causal,
+                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_tensors(q8, k8, vt4, o, lse, B, H, N, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  if (N % kBlockN != 0) return ATTN_ERR_DIMS;
+  // the kernel indexes the scale words of V^T with 32-bit integers (per chunk; all heads bound it)
+  if (static_cast<long long>(B) * H * d * (N / kBlockN) >= (1ll << 32)) return ATTN_ERR_OVERFLOW;
+  if (!q_scale || !k_scale || !vt_scale || !workspace) return ATTN_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
+  HostTensor t[kHostMaxTensors];
+  const int nt = fp4p_host_tensors(t, q8, k8, vt4, q_scale, k_scale, vt_scale, o, lse, N, d);
+  const HostChunking hcfg = host_chunking(B, H, t, nt);
+  if (workspace_bytes < kHostSlots * hcfg.slot_bytes) return ATTN_ERR_WORKSPACE;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  return host_pipeline(t, nt, hcfg, static_cast<long long>(B) * H, workspace, dev, stream,
+                       [&](long long, int hn, uint8_t* const* reg) {
+                         return launch_fp4p(reg[0], reg[1], reg[2], reinterpret_cast<const float*>(reg[3]),
+                                            reinterpret_cast<const float*>(reg[4]), reg[5], reg[6],
+                                            lse ? reinterpret_cast<float*>(reg[7]) : nullptr, hn, N, d, causal,
+                                            scale, dev, stream);
+                       });
+}
+
+size_t attn_fwd_fp4p_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d != 128 || N % kBlockN != 0) return 0;
+  HostTensor t[kHostMaxTensors];
+  const int nt = fp4p_host_tensors(t, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, N, d);
+  return kHostSlots * host_chunking(B, H, t, nt).slot_bytes;
+}
+
+}  // extern "C"
+
+namespace {
+// The Direct-P FP4 forward over BH heads of device tensors (arguments already checked).
+int launch_fp4p(const void* q8, const void* k8, const void* vt4, const float* q_scale, const float* k_scale,
+                const uint8_t* vt_scale, void* o, float* lse, int BH, int N, int d, int causal, float scale, int dev,
+                void* stream) {
+  int rc;
   CUtensorMap mq, mk, mv;
   if ((rc = make_map(&mq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
@@ -804,6 +865,9 @@ int attn_fwd_fp4p(const void* q8, const void* k8, const void* vt4, const float* 
   p.v_scale = reinterpret_cast<const float*>(vt_scale);  // E8M0 words, read as such by the FP4 path
   return launch<ATTN_FP4_D128, false, true>(mq, mk, mv, mq, p, dev, stream);
 }
+}  // namespace
+
+extern "C" {
 
 int attn_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,
                      int Nq, int Nk, int d, int causal, int q_offset, int k_offset, float scale, void* stream) {

@@ -236,6 +236,21 @@ int attn_fwd_fp8_host(const void* q8, const void* k8, const void* v8, const floa
 size_t attn_fwd_fp8_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * attn_fwd_fp4p_host -- attn_fwd_fp4p with its inputs and outputs in HOST memory
+ * (page-locked for full speed), in the layouts of attn_fwd_fp4p, pipelined in
+ * chunks of whole heads as attn_fwd_host; the outputs are bit for bit those of
+ * attn_fwd_fp4p.  workspace: at least attn_fwd_fp4p_host_workspace_bytes(B,H,N,d)
+ * bytes (else ATTN_ERR_WORKSPACE), 256-byte aligned, owned by the caller.
+ * Returns the codes of attn_fwd_fp4p and attn_fwd_host.
+ */
+int attn_fwd_fp4p_host(const void* q8, const void* k8, const void* vt4, const float* q_scale, const float* k_scale,
+                       const uint8_t* vt_scale, void* o, float* lse, int B, int H, int N, int d, int causal,
+                       float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device scratch attn_fwd_fp4p_host needs (0 for invalid arguments). */
+size_t attn_fwd_fp4p_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * attn_fwd_fp4p -- Direct-P FP4 forward (the "Hardware-Aware FP4
  * FlashAttention-4" summary: Direct-P for non-causal inference on Blackwell's
  * FP4 tensor cores).  Q K^T as in attn_fwd_fp8; P V on the FP4 tensor cores with

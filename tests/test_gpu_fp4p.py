@@ -113,3 +113,26 @@ def test_invalid_sizes_launch_nothing():
     assert L.attn_fwd_fp4p_raw(p, p, p, p, p, p, o.data_ptr(), 0, 1, 1, 200, 128, 0, 0.1, s) == -2
     torch.cuda.synchronize()
     assert (o.float() == 7.0).all()
+
+
+@pytest.mark.parametrize("pin", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("shape", [(1, 3, 1024, False), (2, 16, 2048, True)], ids=["B1H3N1024", "B2H16N2048c"])
+def test_host_buffers_bitwise_equal_to_device_call(shape, pin):
+    """attn_fwd_fp4p_host: the same inputs in host memory, pipelined in chunks of
+    whole heads; every chunk runs attn_fwd_fp4p's kernel, so the outputs are bit
+    for bit those of attn_fwd_fp4p."""
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, causal = shape
+    w = synth.make_fp4p(B, H, N, 128, causal, seed=900 + N)
+
+    def host(x):
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        return t.pin_memory() if pin else t.clone()
+    ins = [host(x) for x in (w.q, w.k, w.v, w.q_scale, w.k_scale, w.v_scale)]
+    o_h, l_h = pkg.attn_fwd_fp4p_host(*ins, causal=causal, scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    o_d, l_d = pkg.attn_fwd_fp4p(*[t.cuda() for t in ins], causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h.view(torch.int16), o_d.cpu().view(torch.int16))
+    assert torch.equal(l_h.view(torch.int32), l_d.cpu().view(torch.int32))
+    assert pkg.check_device_errors()[0] == 0
