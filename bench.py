@@ -553,9 +553,9 @@ def main():
 
     # end to end through the public API: pinned host inputs -> device, the pass,
     # its results back to pinned host memory, every step.  Forward: Q, K, V in,
-    # O and LSE out (one attn_fwd_host, attn_fwd_fp8_host or attn_fwd_fp4p_host call,
-    # which pipeline the transfers with the kernels).  Backward: Q, K, V, O, dO, LSE
-    # in, dQ, dK, dV out.
+    # O and LSE out; backward: Q, K, V, O, dO, LSE in, dQ, dK, dV out (one call of
+    # the matching host-buffer entry point, which pipelines the transfers with the
+    # kernels; decode: copies, the pass, copies on one stream).
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
     qd, kd, vd = (torch.empty_like(t) for t in (q, k, v))
     sd = [torch.empty_like(t) for t in scales]
@@ -570,14 +570,19 @@ def main():
         in_host = [q_h, k_h, v_h] + list(sc_h)
     outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
 
-    # the BF16, FP8 and Direct-P FP4 forwards: the library's pipelined host-buffer entry points
-    host_api = not (bwd or decode)
+    # the BF16, FP8 and Direct-P FP4 forwards and the backward: the library's
+    # pipelined host-buffer entry points
+    host_api = not decode
     if host_api:
-        need = (pkg.fp4p_host_workspace_bytes if fp4 else pkg.fp8_host_workspace_bytes if fp8
-                else pkg.fwd_host_workspace_bytes)(w.B, w.H, Nq, w.d)
+        need = (pkg.bwd_host_workspace_bytes if bwd else pkg.fp4p_host_workspace_bytes if fp4
+                else pkg.fp8_host_workspace_bytes if fp8 else pkg.fwd_host_workspace_bytes)(w.B, w.H, Nq, w.d)
         hws = torch.empty(need, dtype=torch.uint8, device=dev)
 
     def e2e_step():
+        if host_api and bwd:
+            pkg.attn_bwd_host(q_h, k_h, v_h, o_in_h, do_h, l_in_h, causal=w.causal, scale=w.scale,
+                              dq=outs_h[0], dk=outs_h[1], dv=outs_h[2], workspace=hws)
+            return
         if host_api and fp4:
             pkg.attn_fwd_fp4p_host(q_h, k_h, v_h, *sc_h, causal=w.causal, scale=w.scale, o=outs_h[0],
                                    lse=outs_h[1], workspace=hws)
@@ -699,7 +704,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": int(sum(t.nbytes for t in in_host)),
                 "d2h_bytes_per_step": int(sum(t.nbytes for t in outs_h)),
-                "api": ((("attn_fwd_fp4p_host" if fp4 else "attn_fwd_fp8_host" if fp8 else "attn_fwd_host")
+                "api": ((("attn_bwd_host" if bwd else "attn_fwd_fp4p_host" if fp4 else "attn_fwd_fp8_host" if fp8
+                          else "attn_fwd_host")
                          + ": pinned host buffers, chunked copies overlapped with the kernels")
                         if host_api else "pinned host copies in, the pass, copies out, on one stream")},
         "gpu_launches": args.steps * launches_per_step,

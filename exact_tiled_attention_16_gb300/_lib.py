@@ -78,6 +78,11 @@ def load_library():
     lib.attn_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
     lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, ctypes.c_size_t, vp]
+    lib.attn_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, ctypes.c_size_t,
+                                  vp]
+    lib.attn_bwd_host.restype = ci
+    lib.attn_bwd_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.attn_bwd_host_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_bwd.restype = ci
     lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -519,6 +524,43 @@ def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
+
+
+def bwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().attn_bwd_host_workspace_bytes(B, H, N, d))
+
+
+def attn_bwd_host(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None,
+                  dv=None, workspace=None, stream=None):
+    """attn_bwd on HOST tensors (bf16 [B,H,N,d], lse float32 [B,H,N]; page-locked
+    for full speed); transfers and kernels are pipelined by the library.  Returns
+    host (dq, dk, dv), valid once `stream` (default: torch's current stream) has
+    completed."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous host bf16 tensor [B,H,N,d]")
+    if any(t.shape != q.shape for t in (k, v, o, dout)):
+        raise ValueError("q, k, v, o and dout must have the same shape [B,H,N,d]")
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be a contiguous host float32 tensor [B,H,N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q.is_pinned()
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dq is None else dq
+    dk = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dk is None else dk
+    dv = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dv is None else dv
+    need = bwd_host_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = load_library().attn_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                      1 if causal else 0, float(scale), workspace.data_ptr(),
+                                      workspace.numel() * workspace.element_size(), _stream_handle(stream) or None)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_host")
     return dq, dk, dv
 
 

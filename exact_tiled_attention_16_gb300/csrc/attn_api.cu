@@ -199,7 +199,7 @@ struct HostTensor {
   void* out;       // host destination (outputs), or null
   size_t per_head;
 };
-constexpr int kHostMaxTensors = 8;
+constexpr int kHostMaxTensors = 12;
 
 struct HostChunking {
   int heads;          // heads per chunk (the last chunk may hold fewer)
@@ -245,6 +245,24 @@ int fp8_host_tensors(HostTensor* t, const void* q8, const void* k8, const void* 
   t[6] = {nullptr, o, 2 * hb};
   t[7] = {nullptr, lse, static_cast<size_t>(N) * sizeof(float)};
   return 8;
+}
+// The backward's tensors: Q, K, V, O, dO, LSE in; dQ, dK, dV out; its scratch
+// (-lse log2e and -scale D per padded row) in the slot only.
+int bwd_host_tensors(HostTensor* t, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int N, int d) {
+  const size_t hb = static_cast<size_t>(N) * d * 2;
+  const size_t npad = (static_cast<size_t>(N) + kBlockM - 1) / kBlockM * kBlockM;
+  t[0] = {q, nullptr, hb};
+  t[1] = {k, nullptr, hb};
+  t[2] = {v, nullptr, hb};
+  t[3] = {o, nullptr, hb};
+  t[4] = {dout, nullptr, hb};
+  t[5] = {lse, nullptr, static_cast<size_t>(N) * sizeof(float)};
+  t[6] = {nullptr, dq, hb};
+  t[7] = {nullptr, dk, hb};
+  t[8] = {nullptr, dv, hb};
+  t[9] = {nullptr, nullptr, 2 * npad * sizeof(float)};
+  return 10;
 }
 // The Direct-P FP4 path's tensors: e4m3 Q, K, e2m1 V^T, the Q and K block scales and
 // the E8M0 scales of V^T in; O, LSE out.
@@ -1001,6 +1019,35 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   bp.err = g_dev[dev].err_ptr;
   if (d == 64) return launch_bwd<ATTN_BWD_D64>(mq, mk, mv, mdo, bp, dev, stream);
   return launch_bwd<ATTN_BWD_D128>(mq, mk, mv, mdo, bp, dev, stream);
+}
+
+int attn_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  int rc = validate_tensors(q, k, v, o, nullptr, B, H, N, N, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (!dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
+  HostTensor t[kHostMaxTensors];
+  const int nt = bwd_host_tensors(t, q, k, v, o, dout, lse, dq, dk, dv, N, d);
+  const HostChunking hcfg = host_chunking(B, H, t, nt);
+  if (workspace_bytes < kHostSlots * hcfg.slot_bytes) return ATTN_ERR_WORKSPACE;
+  int dev = 0;
+  if ((rc = device_setup(&dev)) != ATTN_OK) return rc;
+  return host_pipeline(t, nt, hcfg, static_cast<long long>(B) * H, workspace, dev, stream,
+                       [&](long long, int hn, uint8_t* const* reg) {
+                         return attn_bwd(reg[0], reg[1], reg[2], reg[3], reg[4], reinterpret_cast<const float*>(reg[5]),
+                                         reg[6], reg[7], reg[8], 1, hn, N, d, causal, scale, reg[9],
+                                         hcfg.region[9], stream);
+                       });
+}
+
+size_t attn_bwd_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  HostTensor t[kHostMaxTensors];
+  const int nt = bwd_host_tensors(t, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, N,
+                                  d);
+  return kHostSlots * host_chunking(B, H, t, nt).slot_bytes;
 }
 
 const char* attn_status_string(int status) {

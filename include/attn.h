@@ -251,6 +251,22 @@ int attn_fwd_fp4p_host(const void* q8, const void* k8, const void* vt4, const fl
 size_t attn_fwd_fp4p_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * attn_bwd_host -- attn_bwd with Q, K, V, O, dO, LSE, dQ, dK and dV in HOST memory
+ * (page-locked for full speed), pipelined in chunks of whole heads as
+ * attn_fwd_host (the scratch attn_bwd needs lives in the workspace slots); every
+ * chunk runs attn_bwd on whole heads, so the gradients are bit for bit those of
+ * attn_bwd.  workspace: at least attn_bwd_host_workspace_bytes(B,H,N,d) bytes
+ * (else ATTN_ERR_WORKSPACE), 256-byte aligned, owned by the caller.  Returns the
+ * codes of attn_bwd and attn_fwd_host.
+ */
+int attn_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* Device scratch attn_bwd_host needs (0 for invalid arguments). */
+size_t attn_bwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * attn_fwd_fp4p -- Direct-P FP4 forward (the "Hardware-Aware FP4
  * FlashAttention-4" summary: Direct-P for non-causal inference on Blackwell's
  * FP4 tensor cores).  Q K^T as in attn_fwd_fp8; P V on the FP4 tensor cores with

@@ -201,3 +201,29 @@ def test_workspace_too_small_launches_nothing():
     assert rc == L.ATTN_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert (dq.float() == 7.0).all()
+
+
+@pytest.mark.parametrize("pin", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("shape", [(1, 3, 700, 128, True), (2, 16, 1024, 64, False), (1, 32, 512, 128, True)],
+                         ids=["B1H3N700d128c", "B2H16N1024d64n", "B1H32N512d128c_8_chunks"])
+def test_host_buffers_bitwise_equal_to_device_call(shape, pin):
+    """attn_bwd_host: every tensor in host memory, pipelined in chunks of whole
+    heads (each chunk's scratch in its workspace slot); every chunk runs attn_bwd
+    on whole heads, so the gradients are bit for bit those of attn_bwd."""
+    import exact_tiled_attention_16_gb300 as pkg
+    B, H, N, d, causal = shape
+    w = synth.make_bf16(B, H, N, d, causal, seed=1300 + N)
+    do_bits = synth.make_grad_out(B, H, N, d, seed=1300 + N)
+    q, k, v, do = _dev(w.q), _dev(w.k), _dev(w.v), _dev(do_bits)
+    o, lse = pkg.attn_fwd(q, k, v, causal=causal, scale=w.scale)
+    g_d = pkg.attn_bwd(q, k, v, o, do, lse, causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+
+    def host(t):
+        t = t.cpu()
+        return t.pin_memory() if pin else t
+    g_h = pkg.attn_bwd_host(*(host(t) for t in (q, k, v, o, do, lse)), causal=causal, scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    for a, b in zip(g_h, g_d):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+    assert pkg.check_device_errors()[0] == 0
