@@ -88,8 +88,8 @@ def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = Fa
     instance table of attn_api.cu (D, K stages, V stages, fp8, partial, fp4, the
     TMA store of O, which the non-causal BF16 launches use, the unit table, which
     BF16 launches use when every CTA's rounds fit in it, and the pair tail, a
-    non-causal last round split over CTA pairs: `table` and `pair_tail` from the
-    library's schedule diagnostic)."""
+    non-causal last round split over CTA pairs, in BF16 table launches and FP8
+    launches: `table` and `pair_tail` from the library's schedule diagnostic)."""
     import re
     text = open(os.path.join(CSRC, "attn_api.cu")).read()
     inst = dict(re.findall(r"#define (ATTN_\w+_D\d+) (\d+, \d+, \d+, (?:true|false))", text))
@@ -100,7 +100,7 @@ def kernel_instance(dtype: str, d: int, partial: bool = False, causal: bool = Fa
     fp4 = dtype == "e4m3_e2m1"
     tma_o = dtype == "bf16" and not partial and not causal
     tab = dtype == "bf16" and not partial and table
-    tail = tab and tma_o and pair_tail
+    tail = pair_tail and not partial and ((tab and tma_o) or dtype == "e4m3")
     args = [D, nk, nv, "1" if fp8 == "true" else "0", "1" if partial else "0", "1" if fp4 else "0",
             "1" if tma_o else "0", "1" if tab else "0", "1" if tail else "0"]
     return "attn::attn_fwd_kernel<" + ", ".join(args) + ">"
@@ -638,8 +638,8 @@ def main():
         kname = kernel_instance(w.dtype, w.d, partial=True) + " + attn::attn_merge_kernel"
     else:
         sched = {}
-        if w.dtype == "bf16":
-            sched = pkg.diag_fwd_schedule(w.B * w.H, w.N, w.N, w.causal, d=w.d,
+        if w.dtype in ("bf16", "e4m3"):
+            sched = pkg.diag_fwd_schedule(w.B * w.H, w.N, w.N, w.causal, d=w.d, fp8=w.dtype == "e4m3",
                                           num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)[0]
         kname = kernel_instance(w.dtype, w.d, causal=w.causal, table=bool(sched.get("table")),
                                 pair_tail=bool(sched.get("pair_tail")))

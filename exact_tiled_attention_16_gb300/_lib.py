@@ -626,17 +626,19 @@ ORDER_HEADS, ORDER_ZIGZAG, ORDER_GROUPS = 0, 1, 2
 
 
 def diag_fwd_schedule(BH, Nq, Nk, causal, d=128, num_sms=152, q_offset=0, k_offset=0, kv_key_bytes=None,
-                      table_ok=True):
+                      table_ok=True, fp8=False):
     """The forward kernel's unit schedule for a launch shape (host only, no GPU):
     (info, seq) with info = {order, group_heads, grid, rounds, makespan, table,
     pair_tail} and seq an int32 array [grid, rounds] of unit ids (-3 - unit: the
     odd CTA of a split pair-tail unit, -2: skipped iteration, -1: done).
-    table_ok: a BF16 attn_fwd launch (True) or another entry point."""
+    table_ok: a BF16 attn_fwd launch (True) or another entry point; fp8: an
+    attn_fwd_fp8 launch (K/V bytes per key 2 d unless given)."""
     import numpy as np
-    kv = 4 * d if kv_key_bytes is None else kv_key_bytes
+    kv = (2 * d if fp8 else 4 * d) if kv_key_bytes is None else kv_key_bytes
+    kind = 2 if fp8 else (1 if table_ok else 0)
     lib = load_library()
     info = (ctypes.c_int * 7)()
-    args = (BH, Nq, Nk, int(bool(causal)), q_offset, k_offset, kv, int(bool(table_ok)), num_sms)
+    args = (BH, Nq, Nk, int(bool(causal)), q_offset, k_offset, kv, kind, num_sms)
     rc = lib.attn_diag_fwd_schedule(*args, ctypes.cast(info, ctypes.c_void_p), None, 0)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_diag_fwd_schedule")

@@ -115,6 +115,7 @@ int device_setup(int* dev_out) {
         configure_kernel<ATTN_BF16_D64, true>() != cudaSuccess ||
         configure_kernel<ATTN_BF16_D128, true>() != cudaSuccess ||
         configure_kernel<ATTN_FP8_D128, false>() != cudaSuccess ||
+        configure_kernel<ATTN_FP8_D128, false, false, false, false, true>() != cudaSuccess ||
         configure_kernel<ATTN_FP4_D128, false, true>() != cudaSuccess ||
         configure_bwd<ATTN_BWD_D64>() != cudaSuccess || configure_bwd<ATTN_BWD_D128>() != cudaSuccess ||
         cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_ptr), g_attn_err) != cudaSuccess) {
@@ -383,7 +384,7 @@ std::atomic<bool> g_pair_tail_ok{true};            // attn_diag_set_pair_tail
 
 // table_cap: rounds the unit table of the launch's kTable instance holds (0: the
 // entry point has none)
-void choose_order(FwdParams& p, int num_sms, long long kv_key_bytes, int table_cap) {
+void choose_order(FwdParams& p, int num_sms, long long kv_key_bytes, int table_cap, bool tail_untabled) {
   const bool table_ok = table_cap > 0;
   p.order = kOrderHeads;
   p.group_heads = p.BH;
@@ -400,12 +401,13 @@ void choose_order(FwdParams& p, int num_sms, long long kv_key_bytes, int table_c
     // units of at least kPairTailMinBlocks key blocks (twice that at d = 64, whose
     // blocks take about half the time) are split.
     const int min_kb = kv_key_bytes >= 4 * 128 ? kPairTailMinBlocks : 2 * kPairTailMinBlocks;
-    if (p.sched_table && p.num_splits == 1 && p.num_kblocks >= min_kb && g_pair_tail_ok && num_sms >= 2) {
+    if ((p.sched_table || tail_untabled) && p.num_splits == 1 && p.num_kblocks >= min_kb && g_pair_tail_ok &&
+        num_sms >= 2) {
       FwdParams c = p;
       c.pair_tail = 1;
       const int Gp = grid_for(c, num_sms);
       const int full = p.num_units / Gp, rem = p.num_units - full * Gp;
-      if (rem > 0 && 2 * rem <= Gp && full + 1 <= table_cap) p.pair_tail = 1;
+      if (rem > 0 && 2 * rem <= Gp && (!p.sched_table || full + 1 <= table_cap)) p.pair_tail = 1;
     }
     return;
   }
@@ -483,8 +485,10 @@ void choose_order(FwdParams& p, int num_sms, long long kv_key_bytes, int table_c
 // table_ok: the launch may go to a kTable instance (the BF16 final-output entry
 // points); the table holds kSchedEntries rounds, kSchedEntriesTma in the
 // instances with the O staging buffers (non-causal)
+// tail_untabled: the launch may split its last round over CTA pairs without the
+// unit table (the FP8 entry points, whose instances compute their units)
 void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset, int k_offset, int num_splits,
-                 float scale, int num_sms, long long kv_key_bytes, bool table_ok) {
+                 float scale, int num_sms, long long kv_key_bytes, bool table_ok, bool tail_untabled = false) {
   std::memset(&p, 0, sizeof(p));
   p.BH = BH;
   p.Nq = Nq;
@@ -498,7 +502,8 @@ void fill_params(FwdParams& p, int BH, int Nq, int Nk, int causal, int q_offset,
   p.num_splits = sp.num_splits;
   p.num_units = BH * p.num_pairs * p.num_splits;
   p.causal = causal ? 1 : 0;
-  choose_order(p, num_sms, kv_key_bytes, !table_ok ? 0 : (causal ? kSchedEntries : kSchedEntriesTma));
+  choose_order(p, num_sms, kv_key_bytes, !table_ok ? 0 : (causal ? kSchedEntries : kSchedEntriesTma),
+               tail_untabled);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns;
 }
@@ -797,13 +802,14 @@ int launch_fp8(const void* q8, const void* k8, const void* v8, const float* q_sc
   if ((rc = make_map(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   if ((rc = make_map(&mv, v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128)) != ATTN_OK) return rc;
   FwdParams p;
-  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 2ll * d, false);
+  fill_params(p, BH, N, N, causal, 0, 0, 1, scale, g_dev[dev].num_sms, 2ll * d, false, true);
   p.err = g_dev[dev].err_ptr;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  if (p.pair_tail) return launch<ATTN_FP8_D128, false, false, false, false, true>(mq, mk, mv, mq, p, dev, stream);
   return launch<ATTN_FP8_D128, false>(mq, mk, mv, mq, p, dev, stream);
 }
 }  // namespace
@@ -1121,14 +1127,16 @@ extern "C" int attn_diag_force_fwd_order(int order, int group_heads) {
 }
 
 extern "C" int attn_diag_fwd_schedule(int BH, int Nq, int Nk, int causal, int q_offset, int k_offset,
-                                      long long kv_key_bytes, int table_ok, int num_sms, int* info, int* seq,
+                                      long long kv_key_bytes, int launch_kind, int num_sms, int* info, int* seq,
                                       long long seq_len) {
   if (!info) return ATTN_ERR_NULL;
-  if (BH < 1 || Nq < 1 || Nk < 1 || num_sms < 1 || kv_key_bytes < 1) return ATTN_ERR_DIMS;
+  if (BH < 1 || Nq < 1 || Nk < 1 || num_sms < 1 || kv_key_bytes < 1 || launch_kind < 0 || launch_kind > 2)
+    return ATTN_ERR_DIMS;
   const long long qblocks = (static_cast<long long>(Nq) + kBlockM - 1) / kBlockM;
   if (Nq >= kMaxSeq || Nk >= kMaxSeq || static_cast<long long>(BH) * qblocks > INT_MAX) return ATTN_ERR_OVERFLOW;
   FwdParams p;
-  fill_params(p, BH, Nq, Nk, causal, q_offset, k_offset, 1, 1.f, num_sms, kv_key_bytes, table_ok != 0);
+  fill_params(p, BH, Nq, Nk, causal, q_offset, k_offset, 1, 1.f, num_sms, kv_key_bytes, launch_kind == 1,
+              launch_kind == 2);
   const int G = grid_for(p, num_sms);
   int rounds = 0;
   for (int c = 0; c < G; ++c) {

@@ -352,7 +352,7 @@ __host__ __device__ __forceinline__ int tail_role(int round, const FwdParams& p,
 // when every CTA's rounds fit in the table.  The others compute it here, and
 // the host gives them only the head-major and zigzag orders, whose arithmetic
 // is short.
-template <int kN>
+template <int kN, bool kTail = false>
 __device__ __forceinline__ int next_unit(int round, const SchedEntry* tab, const FwdParams& p, UnitInfo& ui) {
   if constexpr (kN > 0) {
     if (round >= kN) return kNoMoreUnits;
@@ -367,7 +367,7 @@ __device__ __forceinline__ int next_unit(int round, const SchedEntry* tab, const
     return e.u;
   } else {
     const int u = unit_for_round<false>(round, p, gridDim.x, blockIdx.x);
-    if (u >= 0) ui = unit_info(u, p);
+    if (u >= 0) ui = unit_info(u, p, kTail ? tail_role(round, p, gridDim.x, blockIdx.x) : 0);
     return u;
   }
 }
@@ -422,7 +422,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   static_assert(!kFp4 || (kFp8 && D == 128 && !kPartial), "Direct-P FP4: e4m3 Q K^T, d = 128, final output");
   static_assert(!kTmaO || !kPartial, "the TMA store serves the final bf16 output");
   using Plan = SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>;
-  static_assert(!kPairTail || (kTable && !kPartial && !kFp8), "the pair tail serves BF16 table launches");
+  static_assert(!kPairTail || (!kPartial && !kFp4 && (kTable || kFp8)),
+                "the pair tail serves BF16 table launches and FP8 launches");
   using L = typename Plan::In;
   using LV = typename Plan::V16;
   constexpr uint32_t kTmemS[2] = {0, 128};
@@ -541,7 +542,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       bool ok = true;
       for (int round = 0; ok; ++round) {
         UnitInfo ui;
-        const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
+        const int u = next_unit<Plan::kSchedN, kPairTail>(round, sched, p, ui);
         if (u == kNoMoreUnits) break;
         if (u == kSkipRound) continue;
         const int nkv = ui.n[1];
@@ -653,7 +654,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       bool merges = false;     // pair tail: this CTA receives its partner's half
       for (int round = 0; ok; ++round) {
         UnitInfo ui;
-        const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
+        const int u = next_unit<Plan::kSchedN, kPairTail>(round, sched, p, ui);
         if (u == kNoMoreUnits) break;
         if (u == kSkipRound) continue;
         merges = merges || ui.role == 1;
@@ -759,7 +760,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       bool ok = true;
       for (int round = 0; ok; ++round) {
         UnitInfo ui;
-        const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
+        const int u = next_unit<Plan::kSchedN, kPairTail>(round, sched, p, ui);
         if (u == kNoMoreUnits) break;
         if (u == kSkipRound) continue;
         const int nkv = ui.n[1];
@@ -805,12 +806,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const uint32_t tO = tmem + lane_addr + kTmemO[t];
     uint32_t s_iter = 0, pv_iter = 0;
     uint32_t ost_uses = 0;  // TMA stores of O issued from this tile's staging chunk
-    int tail_role = 0, tail_bh = 0, tail_row = 0;  // pair tail: this CTA's split half
-    float tail_m = 0.f, tail_l = 0.f;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       UnitInfo ui;
-      const int u = next_unit<Plan::kSchedN>(round, sched, p, ui);
+      const int u = next_unit<Plan::kSchedN, kPairTail>(round, sched, p, ui);
       if (u == kNoMoreUnits) break;
       if (u == kSkipRound) continue;
       const int bh = ui.bh;
@@ -1031,17 +1030,70 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         ++pv_iter;
         tc_fence_after();
         if constexpr (kPairTail) {
-          // the pair-tail half is always the CTA's last unit: its epilogue follows
-          // the loop.  The role is read again from the table here (a volatile
-          // load), so that no register carries it through the block loop.
-          const int role = reinterpret_cast<volatile const SchedEntry*>(sched)[round].role;
+          // The role is read again here (from the table, a volatile load, or
+          // computed), so that no register carries it through the block loop, and
+          // the exchange runs right here, so that nothing is carried out of the loop
+          // either (either spilled the 216-register softmax warps).
+          int role;
+          if constexpr (kTable) role = reinterpret_cast<volatile const SchedEntry*>(sched)[round].role;
+          else role = tail_role(round, p, gridDim.x, blockIdx.x);
           if (role != 0) {
-            tail_role = role;
-            tail_bh = bh;
-            tail_row = row;
-            tail_m = m_use;
-            tail_l = l;
-            break;
+            const float osc = kFp8 ? sv_max * (1.f / 64.f) : 1.f;  // O' -> unnormalised O (FP8: pre-scale, V scales)
+            // Pair tail: the odd CTA sends its half (O_t unnormalised, m, l per
+            // row) into the even CTA's Q/K/V regions (FP8: and its f16 copies of
+            // V); the even CTA merges the two halves the way split-K/V partials
+            // merge, normalises and stores.  Row layout: [m, l, pad, pad, O_0 ..
+            // O_{D-1}] in fp32, a 16-byte-aligned pitch whose 16-byte units fall in
+            // different bank groups for 8 consecutive rows.  O_t moves 32 columns
+            // at a time (few live registers).
+            constexpr uint32_t kRowBytes = (D + 4) * 4;
+            static_assert(2 * kBlockM * kRowBytes <= Plan::kOst,
+                          "pair-tail rows exceed the Q, K, V (and f16 V) regions");
+            const uint32_t my_row = base + Plan::kQ + (t * kBlockM + row_in_tile) * kRowBytes;
+            const uint32_t peer = cluster_ctarank() ^ 1u;
+            if (role == 2) {
+              if (warp_wait_cluster(b_recv_ready, 0, abort_flag, tmo, p.err, 32)) {
+                const uint32_t dst = mapa_shared(my_row, peer);
+                st_cluster_v2(dst, m_use, l);  // (a four-wide store with two zero words spilled registers)
+                for (int h = 0; h < D / 32; ++h) {
+                  uint32_t oraw[32];
+                  tmem_ld32_wait(tO + 32 * h, oraw);
+#pragma unroll
+                  for (int v = 0; v < 8; ++v)
+                    st_cluster_v4(dst + 16 + (32 * h + 4 * v) * 4, __uint_as_float(oraw[4 * v]) * osc,
+                                  __uint_as_float(oraw[4 * v + 1]) * osc, __uint_as_float(oraw[4 * v + 2]) * osc,
+                                  __uint_as_float(oraw[4 * v + 3]) * osc);
+                }
+                mbar_arrive_cluster(mapa_shared(b_data_ready + 8 * t, peer));
+              }
+            } else if (warp_wait_cluster(b_data_ready + 8 * t, 0, abort_flag, tmo, p.err, 33 + t)) {
+              const float4 ml = ld_shared_v4f(my_row);
+              const float m = fmaxf(m_use, ml.x);
+              const float a0 = m_use == -INFINITY ? 0.f : ex2_approx(m_use - m);
+              const float a1 = ml.x == -INFINITY ? 0.f : ex2_approx(ml.x - m);
+              const float lt = l * a0 + ml.y * a1;
+              const float w0 = a0 * osc / lt, w1 = a1 / lt;
+              uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.Nq + row) * D);
+              for (int h = 0; h < D / 32; ++h) {
+                uint32_t oraw[32];
+                tmem_ld32_wait(tO + 32 * h, oraw);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const float4 x0 = ld_shared_v4f(my_row + 16 + (32 * h + 8 * v) * 4);
+                  const float4 x1 = ld_shared_v4f(my_row + 16 + (32 * h + 8 * v + 4) * 4);
+                  const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                  uint32_t w[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * w0 + xs[2 * e] * w1,
+                                       __uint_as_float(oraw[8 * v + 2 * e + 1]) * w0 + xs[2 * e + 1] * w1);
+                  if (row < p.Nq) dst[4 * h + v] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+              }
+              if (row < p.Nq && p.lse != nullptr)
+                p.lse[static_cast<size_t>(bh) * p.Nq + row] = (m + lg2_approx(lt)) * 0.69314718055994530942f;
+            }
+            continue;
           }
         }
         const float inv_l = ((kFp8 && !kFp4) ? sv_max * (1.f / 64.f) : 1.f) / l;
@@ -1144,62 +1196,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             dst[v] = make_float4(__uint_as_float(oraw[4 * v]) * inv_l, __uint_as_float(oraw[4 * v + 1]) * inv_l,
                                  __uint_as_float(oraw[4 * v + 2]) * inv_l, __uint_as_float(oraw[4 * v + 3]) * inv_l);
           p.lse_part[rp] = empty ? -INFINITY : (m_use + lg2_approx(l)) * 0.69314718055994530942f;
-        }
-      }
-    }
-    if constexpr (kPairTail) {
-      if (ok && tail_role != 0) {
-        // Pair tail: the odd CTA sends its half (O_t unnormalised, m, l per row)
-        // into the even CTA's Q/K/V regions; the even CTA merges the two halves
-        // the way split-K/V partials merge, normalises and stores.  Row layout:
-        // [m, l, 0, 0, O_0 .. O_{D-1}] in fp32, a 16-byte-aligned pitch whose
-        // 16-byte units fall in different bank groups for 8 consecutive rows.
-        // O_t moves 32 columns at a time (few live registers).
-        constexpr uint32_t kRowBytes = (D + 4) * 4;
-        static_assert(2 * kBlockM * kRowBytes <= Plan::kC, "pair-tail rows exceed the Q, K and V regions");
-        const uint32_t my_row = base + Plan::kQ + (t * kBlockM + row_in_tile) * kRowBytes;
-        const uint32_t peer = cluster_ctarank() ^ 1u;
-        if (tail_role == 2) {
-          if (warp_wait_cluster(b_recv_ready, 0, abort_flag, tmo, p.err, 32)) {
-            const uint32_t dst = mapa_shared(my_row, peer);
-            st_cluster_v4(dst, tail_m, tail_l, 0.f, 0.f);
-            for (int h = 0; h < D / 32; ++h) {
-              uint32_t oraw[32];
-              tmem_ld32_wait(tO + 32 * h, oraw);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                st_cluster_v4(dst + 16 + (32 * h + 4 * v) * 4, __uint_as_float(oraw[4 * v]),
-                              __uint_as_float(oraw[4 * v + 1]), __uint_as_float(oraw[4 * v + 2]),
-                              __uint_as_float(oraw[4 * v + 3]));
-            }
-            mbar_arrive_cluster(mapa_shared(b_data_ready + 8 * t, peer));
-          }
-        } else if (warp_wait_cluster(b_data_ready + 8 * t, 0, abort_flag, tmo, p.err, 33 + t)) {
-          const float4 ml = ld_shared_v4f(my_row);
-          const float m = fmaxf(tail_m, ml.x);
-          const float a0 = tail_m == -INFINITY ? 0.f : ex2_approx(tail_m - m);
-          const float a1 = ml.x == -INFINITY ? 0.f : ex2_approx(ml.x - m);
-          const float lt = tail_l * a0 + ml.y * a1;
-          const float w0 = a0 / lt, w1 = a1 / lt;
-          uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(tail_bh) * p.Nq + tail_row) * D);
-          for (int h = 0; h < D / 32; ++h) {
-            uint32_t oraw[32];
-            tmem_ld32_wait(tO + 32 * h, oraw);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const float4 x0 = ld_shared_v4f(my_row + 16 + (32 * h + 8 * v) * 4);
-              const float4 x1 = ld_shared_v4f(my_row + 16 + (32 * h + 8 * v + 4) * 4);
-              const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(oraw[8 * v + 2 * e]) * w0 + xs[2 * e] * w1,
-                                   __uint_as_float(oraw[8 * v + 2 * e + 1]) * w0 + xs[2 * e + 1] * w1);
-              if (tail_row < p.Nq) dst[4 * h + v] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-          if (tail_row < p.Nq && p.lse != nullptr)
-            p.lse[static_cast<size_t>(tail_bh) * p.Nq + tail_row] = (m + lg2_approx(lt)) * 0.69314718055994530942f;
         }
       }
     }

@@ -220,8 +220,10 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
  * [B,H,ceil(N/128)] in, O bf16 [B,H,N,d] and LSE fp32 [B,H,N] (may be NULL) out.
  * The heads go through the device in up to eight chunks with the copies of one
  * chunk and the kernel of another on separate streams, as attn_fwd_host; each
- * chunk runs attn_fwd_fp8's kernel on whole heads, so the outputs are bit for
- * bit those of attn_fwd_fp8.
+ * chunk runs attn_fwd_fp8's kernel on whole heads, so the outputs equal those of
+ * attn_fwd_fp8 up to rounding (a launch whose last round is split over CTA pairs
+ * merges two key halves, as in attn_fwd_host), bit for bit with the split off
+ * (attn_diag_set_pair_tail(0)).
  *   workspace : device scratch of at least attn_fwd_fp8_host_workspace_bytes(B,H,N,d)
  *               bytes (else ATTN_ERR_WORKSPACE), 256-byte aligned, owned by the
  *               caller; the call overwrites it
@@ -380,10 +382,12 @@ int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, float* 
  * their work units for a launch of BH heads of Nq query rows over Nk keys
  * (causal: 0/1; q_offset, k_offset: positions of the first query row and key,
  * as in attn_fwd_partial; kv_key_bytes: bytes of one key's K and V rows, 4 d for
- * BF16, 2 d for e4m3) on num_sms SMs, one key range per unit.  table_ok: 1 for
- * a launch of attn_fwd / attn_fwd_host (BF16), whose causal launches may take
- * their units from a table in shared memory and then use any order; 0 for the
- * other entry points (head-major or zigzag only).
+ * BF16, 2 d for e4m3) on num_sms SMs, one key range per unit.  launch_kind: 1
+ * for a launch of attn_fwd / attn_fwd_host (BF16), whose causal launches may take
+ * their units from a table in shared memory and then use any order; 2 for
+ * attn_fwd_fp8 / attn_fwd_fp8_host, which compute their units (head-major or
+ * zigzag only) and may split their last round over CTA pairs; 0 for the other
+ * entry points (computed units, head-major or zigzag, no split).
  * A unit is a pair of 128-row query tiles of one head: id = head * P + r with
  * P = ceil(Nq / 256) pairs per head; under the causal mask r = 0 is the heaviest
  * pair (the last rows), otherwise the first.
@@ -397,11 +401,11 @@ int attn_diag_tmem_row_max(const float* in, float* vals, float* row_max, float* 
  * c takes in its r-th iteration (-3 - unit for the odd CTA of a split unit), -2
  * for an iteration it skips, -1 once it is done; seq_len: its capacity in ints
  * (else ATTN_ERR_WORKSPACE).
- * Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_DIMS, ATTN_ERR_OVERFLOW or
- * ATTN_ERR_WORKSPACE.
+ * Returns ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_DIMS (also for launch_kind outside
+ * 0..2), ATTN_ERR_OVERFLOW or ATTN_ERR_WORKSPACE.
  */
 int attn_diag_fwd_schedule(int BH, int Nq, int Nk, int causal, int q_offset, int k_offset, long long kv_key_bytes,
-                           int table_ok, int num_sms, int* info, int* seq, long long seq_len);
+                           int launch_kind, int num_sms, int* info, int* seq, long long seq_len);
 
 /*
  * attn_diag_force_fwd_order -- diagnostics (no counterpart on the pages): makes

@@ -17,8 +17,8 @@ def test_kernel_instance_follows_the_instance_table():
     text = open(os.path.join(bench.CSRC, "attn_api.cu")).read()
     assert "#define ATTN_BF16_D128 128, 2, 2, false" in text
     # D, K stages, V stages, fp8, partial, fp4, TMA store of O (non-causal BF16 only),
-    # unit table (BF16 launches whose rounds fit in it), pair tail (non-causal table
-    # launches that split their last round over CTA pairs)
+    # unit table (BF16 launches whose rounds fit in it), pair tail (non-causal BF16
+    # table launches and FP8 launches that split their last round over CTA pairs)
     assert bench.kernel_instance("bf16", 128, causal=True) == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 0, 0>"
     assert (bench.kernel_instance("bf16", 128, causal=True, table=True)
             == "attn::attn_fwd_kernel<128, 2, 2, 0, 0, 0, 0, 1, 0>")
@@ -34,6 +34,11 @@ def test_kernel_instance_follows_the_instance_table():
     assert bench.kernel_instance("e4m3", 128) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0, 0>"
     assert bench.kernel_instance("e4m3_e2m1", 128) == "attn::attn_fwd_kernel<128, 4, 4, 1, 0, 1, 0, 0, 0>"
     assert bench.kernel_instance("e4m3", 128, causal=True, table=True) == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0, 0>"
+    # FP8 launches compute their units but may split their last round
+    assert (bench.kernel_instance("e4m3", 128, pair_tail=True)
+            == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0, 1>")
+    assert (bench.kernel_instance("e4m3_e2m1", 128, pair_tail=True)
+            == "attn::attn_fwd_kernel<128, 4, 4, 1, 0, 1, 0, 0, 0>")
 
 
 def test_kernel_hash_covers_every_cuda_source(tmp_path, monkeypatch):

@@ -83,6 +83,51 @@ def test_fp8_deterministic():
     assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 6200), (1, 16, 8192)], ids=["ragged_every_unit_split", "B1H16N8192_tail_of_56"])
+def test_fp8_pair_tail(shape):
+    """FP8 launches whose last round is split over CTA pairs: each half carries its
+    own largest V block scale, so the sender rescales its O to the unscaled sum
+    before the merge.  Rows against the oracle (all of them in the ragged case,
+    O and LSE inside guard regions that must stay intact), and the result against
+    the same launch with the split turned off."""
+    import exact_tiled_attention_16_gb300 as pkg
+    import exact_tiled_attention_16_gb300._lib as L
+    B, H, N = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if not pkg.diag_fwd_schedule(B * H, N, N, False, fp8=True, num_sms=sms)[0]["pair_tail"]:
+        pytest.skip(f"{sms} SMs: this shape's last round is not split")
+    w = synth.make_fp8(B, H, N, 128, False, seed=900 + N)
+    q8, k8, v8 = to_device(w)
+    qs, ks, vs = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (w.q_scale, w.k_scale, w.v_scale))
+    n_o, n_l, guard = B * H * N * 128, B * H * N, 4096
+    o_buf = torch.full((n_o + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((n_l + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+    o_view, l_view = o_buf[guard:guard + n_o], l_buf[guard:guard + n_l]
+    rc = L.attn_fwd_fp8_raw(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), qs.data_ptr(), ks.data_ptr(), vs.data_ptr(),
+                            o_view.data_ptr(), l_view.data_ptr(), B, H, N, 128, False, w.scale,
+                            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert pkg.check_device_errors()[0] == 0
+    assert torch.isnan(o_buf[:guard].float()).all() and torch.isnan(o_buf[-guard:].float()).all()
+    assert torch.isnan(l_buf[:guard]).all() and torch.isnan(l_buf[-guard:]).all()
+    o = o_view.view(B, H, N, 128).float().cpu().numpy().astype(np.float64)
+    lse = l_view.view(B, H, N).cpu().numpy().astype(np.float64)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    rows = None if B * H * N <= 20000 else 128
+    det = {}
+    assert_fp8_tol(compare_rows(w, o, lse, rows_per_head=rows, excess=True, detail=det), f"fp8 pair tail {shape}", det)
+    pkg.diag_set_pair_tail(False)
+    try:
+        o2, lse2 = run_fp8(w)
+    finally:
+        pkg.diag_set_pair_tail(True)
+    # the two launches sum the keys in a different order: at most one bf16 step of
+    # the output (2^-7 |O|, up to 0.125 for the |O| ~ 20 rows of the x10 V channels)
+    # beyond the BF16 test's 2e-2
+    assert (np.abs(o - o2) <= 2e-2 + 2.0 ** -7 * np.abs(o2)).all() and np.abs(lse - lse2).max() <= 1e-3
+
+
 def test_fp8_rejects_bad_arguments():
     import exact_tiled_attention_16_gb300._lib as L
     q = torch.zeros(1, 1, 128, 64, dtype=torch.uint8, device="cuda")

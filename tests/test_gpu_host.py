@@ -107,8 +107,9 @@ FP8_SHAPES = [(1, 2, 1000, 128, False), (2, 9, 700, 128, True), (1, 32, 2048, 12
 @pytest.mark.parametrize("shape", FP8_SHAPES, ids=[f"B{b}H{h}N{n}{'c' if c else 'n'}" for b, h, n, d, c in FP8_SHAPES])
 def test_fp8_host_bitwise_equal_to_device_call(shape, pin):
     """attn_fwd_fp8_host: the e4m3 codes and block scales in host memory, pipelined
-    in chunks of whole heads; every chunk runs attn_fwd_fp8's kernel, which never
-    splits a unit, so the outputs are bit for bit those of attn_fwd_fp8."""
+    in chunks of whole heads; every chunk runs attn_fwd_fp8's kernel, so with the
+    split of a last round over CTA pairs off (these shapes have too few key blocks
+    for it anyway) the outputs are bit for bit those of attn_fwd_fp8."""
     import exact_tiled_attention_16_gb300 as pkg
     B, H, N, d, causal = shape
     w = synth.make_fp8(B, H, N, d, causal, seed=700 + N)
@@ -117,11 +118,15 @@ def test_fp8_host_bitwise_equal_to_device_call(shape, pin):
         t = torch.from_numpy(np.ascontiguousarray(x))
         return t.pin_memory() if pin else t.clone()
     q8, k8, v8, qs, ks, vs = (host(x) for x in (w.q, w.k, w.v, w.q_scale, w.k_scale, w.v_scale))
-    o_h, l_h = pkg.attn_fwd_fp8_host(q8, k8, v8, qs, ks, vs, causal=causal, scale=w.scale)
-    torch.cuda.current_stream().synchronize()
-    o_d, l_d = pkg.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qs.cuda(), ks.cuda(), vs.cuda(), causal=causal,
-                                scale=w.scale)
-    torch.cuda.synchronize()
+    pkg.diag_set_pair_tail(False)
+    try:
+        o_h, l_h = pkg.attn_fwd_fp8_host(q8, k8, v8, qs, ks, vs, causal=causal, scale=w.scale)
+        torch.cuda.current_stream().synchronize()
+        o_d, l_d = pkg.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qs.cuda(), ks.cuda(), vs.cuda(),
+                                    causal=causal, scale=w.scale)
+        torch.cuda.synchronize()
+    finally:
+        pkg.diag_set_pair_tail(True)
     assert torch.equal(o_h.view(torch.int16), o_d.cpu().view(torch.int16))
     assert torch.equal(l_h.view(torch.int32), l_d.cpu().view(torch.int32))
     assert pkg.check_device_errors()[0] == 0

@@ -175,6 +175,34 @@ def test_pair_tail_only_when_the_last_round_fits_the_pairs():
     assert pkg.diag_fwd_schedule(32, 4096, 4096, False)[0]["pair_tail"] == 1
 
 
+@pytest.mark.parametrize("shape", [(16, 8192), (2, 6200), (7, 6400), (32, 8192), (16, 16384)])
+def test_fp8_pair_tail(shape):
+    """attn_fwd_fp8 computes its units (no table, head-major for non-causal) and
+    splits its last round the same way when it fits the pairs; its K/V rows are
+    2 d bytes a key, so it wants at least 48 key blocks, like d = 64."""
+    BH, N = shape
+    P = (N + 255) // 256
+    U = BH * P
+    info, seq = pkg.diag_fwd_schedule(BH, N, N, False, fp8=True)
+    assert info["table"] == 0 and info["order"] == HEADS
+    G = info["grid"]
+    full, rem = divmod(U, G)
+    want = 0 < rem <= G // 2 and N >= 48 * 128
+    assert info["pair_tail"] == int(want)
+    units = np.concatenate([seq[seq >= 0]])
+    assert np.array_equal(np.sort(units), np.arange(U))
+    if want:
+        assert np.array_equal(seq[1::2, full][:rem], -3 - np.arange(full * G, U))
+    # too few key blocks, causal, or pair tail switched off: whole units
+    assert pkg.diag_fwd_schedule(32, 4096, 4096, False, fp8=True)[0]["pair_tail"] == 0
+    assert pkg.diag_fwd_schedule(BH, N, N, True, fp8=True)[0]["pair_tail"] == 0
+    pkg.diag_set_pair_tail(False)
+    try:
+        assert pkg.diag_fwd_schedule(BH, N, N, False, fp8=True)[0]["pair_tail"] == 0
+    finally:
+        pkg.diag_set_pair_tail(True)
+
+
 def test_noncausal_and_bad_arguments():
     pkg.diag_set_pair_tail(False)
     try:
