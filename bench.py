@@ -53,7 +53,7 @@ CSRC = os.path.join(ROOT, "exact_tiled_attention_16_gb300", "csrc")
 # 64 cycles (measured), 8192 flops per cycle; the e4m3 Q K^T at the nominal 2x
 ALL_WORKLOADS = ["cfg1", "cfg2n", "cfg2c", "cfg3", "cfg4", "cfg5", "cfg5p", "decode",
                  "custom:1,32,4096,128,0", "custom:1,32,8192,128,0", "custom:1,32,16384,128,0",
-                 "bwd:cfg3", "bwd:cfg4"]
+                 "custom:1,16,8192,128,0,e4m3", "bwd:cfg3", "bwd:cfg4"]
 BF16_FLOP_PER_CLK_SM = 8192.0
 FP8_FLOP_PER_CLK_SM = 16384.0
 WORKLOAD_TEXT = {
@@ -217,8 +217,16 @@ def _blas_threads() -> int:
 def make_workload(args):
     """The synthetic workload the flags name (seeded; see synth.py)."""
     if args.custom:
-        B, H, N, d, c = (int(x) for x in args.custom.split(","))
-        return synth.make_bf16(B, H, N, d, bool(c), seed=3, name=f"custom_B{B}H{H}N{N}d{d}{'c' if c else 'n'}")
+        f = args.custom.split(",")
+        B, H, N, d, c = (int(x) for x in f[:5])
+        kind = f[5] if len(f) > 5 else "bf16"
+        name = f"custom_B{B}H{H}N{N}d{d}{'c' if c else 'n'}"
+        if kind == "e4m3":  # cfg5's recipe (outlier channels x10, rotated Q/K) on another shape
+            return synth.make_fp8(B, H, N, d, bool(c), seed=3, outlier_frac=0.01, outlier_mult=10.0,
+                                  name=name + "_e4m3")
+        if kind != "bf16":
+            raise SystemExit(f"--custom: unknown element type {kind!r} (bf16 or e4m3)")
+        return synth.make_bf16(B, H, N, d, bool(c), seed=3, name=name)
     if args.workload == "decode":
         return make_decode_workload()
     return synth.make_config(args.workload)
@@ -423,11 +431,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="(reference arm only) a small sample workload")
     ap.add_argument("--custom", default=None,
-                    help="B,H,N,d,causal: a seeded bf16 workload of that shape instead of --workload "
-                         "(for profiling captures on a reduced case)")
+                    help="B,H,N,d,causal[,e4m3]: a seeded bf16 (or block-scaled e4m3, cfg5's recipe) "
+                         "workload of that shape instead of --workload (for profiling captures on a "
+                         "reduced case)")
     ap.add_argument("--all", action="store_true",
-                    help="one JSON line for each workload (BASELINE configs, Direct-P, decode, the non-causal "
-                         "d=128 points N=4096/8192/16384, the backward of cfg3 and cfg4)")
+                    help="one JSON line for each workload (cfg1-cfg5, Direct-P, decode, the non-causal "
+                         "d=128 points N=4096/8192/16384, FP8 B1 H16 N8192 (its last round split over CTA "
+                         "pairs), the backward of cfg3 and cfg4)")
     ap.add_argument("--cpu-row-probe", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--probe-rows", type=int, default=256, help=argparse.SUPPRESS)
     args = ap.parse_args()
