@@ -132,6 +132,34 @@ def test_fp8_host_bitwise_equal_to_device_call(shape, pin):
     assert pkg.check_device_errors()[0] == 0
 
 
+def test_fp8_host_with_pair_tail():
+    """B1 H16 N8192: every chunk of the pipeline (two heads, 64 units) splits all its
+    units over CTA pairs, the whole-tensor launch only its last round; both against
+    the oracle on sampled rows, and against each other within one bf16 step of O."""
+    import exact_tiled_attention_16_gb300 as pkg
+    from tests.gpu_utils import assert_fp8_tol, compare_rows
+    B, H, N = 1, 16, 8192
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if not pkg.diag_fwd_schedule(2, N, N, False, fp8=True, num_sms=sms)[0]["pair_tail"]:
+        pytest.skip(f"{sms} SMs: a chunk's units are not split")
+    w = synth.make_fp8(B, H, N, 128, False, seed=4242)
+    q8, k8, v8, qs, ks, vs = (torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+                              for x in (w.q, w.k, w.v, w.q_scale, w.k_scale, w.v_scale))
+    o_h, l_h = pkg.attn_fwd_fp8_host(q8, k8, v8, qs, ks, vs, causal=False, scale=w.scale)
+    torch.cuda.current_stream().synchronize()
+    o_d, l_d = pkg.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qs.cuda(), ks.cuda(), vs.cuda(), causal=False,
+                                scale=w.scale)
+    torch.cuda.synchronize()
+    assert pkg.check_device_errors()[0] == 0
+    o_h = o_h.float().numpy().astype(np.float64)
+    o_d = o_d.float().cpu().numpy().astype(np.float64)
+    l_h = l_h.numpy().astype(np.float64)
+    l_d = l_d.cpu().numpy().astype(np.float64)
+    assert (np.abs(o_h - o_d) <= 2e-2 + 2.0 ** -7 * np.abs(o_d)).all() and np.abs(l_h - l_d).max() <= 1e-3
+    det = {}
+    assert_fp8_tol(compare_rows(w, o_h, l_h, rows_per_head=64, excess=True, detail=det), "fp8 host, pair tail", det)
+
+
 def test_fp8_host_workspace_too_small_launches_nothing():
     import exact_tiled_attention_16_gb300._lib as L
     B, H, N, d = 1, 2, 256, 128
