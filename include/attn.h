@@ -85,6 +85,10 @@ typedef enum { ATTN_BF16 = 0 } attn_dtype;
  *   stream  : cudaStream_t
  * Arithmetic: bf16 Q K^T and P V on the tensor cores with fp32 accumulation,
  * softmax in fp32 with P rounded to bf16, O rounded to bf16 (nearest-even).
+ * Deterministic: the same inputs and shape give the same bits on every call.  A
+ * non-causal launch whose last round of work units holds at most one unit per
+ * pair of CTAs splits those units' keys over two CTAs (a cluster) and merges the
+ * halves (attn_diag_fwd_schedule shows it; attn_diag_set_pair_tail(0) turns it off).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              int causal, float scale, int dtype, void* stream);
@@ -102,7 +106,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * Arithmetic: e4m3 Q K^T on the FP8 tensor cores (fp32 accumulation), softmax in
  * fp32 on the dequantised scores; P rounded to f16 and V's e4m3 codes widened
  * exactly to f16 on chip, P V on the 16-bit tensor path (an e4m3 P loses too much
- * once V has outlier channels); O rounded to bf16.
+ * once V has outlier channels); O rounded to bf16.  Deterministic, and non-causal
+ * launches may split their last round over CTA pairs, as attn_fwd.
  */
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
                  const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
