@@ -216,5 +216,15 @@ def test_noncausal_and_bad_arguments():
     assert np.array_equal(np.sort(seq[seq >= 0]), np.arange(4 * 4))
     with pytest.raises(pkg.AttnError):
         pkg.diag_fwd_schedule(0, 10, 10, True)
+    # a launch kind outside 0 (other entry points), 1 (BF16), 2 (FP8)
+    import ctypes
+    import exact_tiled_attention_16_gb300._lib as L
+    info = (ctypes.c_int * 7)()
+    lib = pkg.load_library()
+    for kind in (-1, 3):
+        assert lib.attn_diag_fwd_schedule(4, 1000, 1000, 0, 0, 0, 512, kind, 152,
+                                          ctypes.cast(info, ctypes.c_void_p), None, 0) == L.ATTN_ERR_DIMS
+    assert lib.attn_diag_fwd_schedule(4, 1000, 1000, 0, 0, 0, 512, 2, 152,
+                                      ctypes.cast(info, ctypes.c_void_p), None, 0) == 0
     with pytest.raises(pkg.AttnError):
         pkg.diag_force_fwd_order(5, 0)
