@@ -518,6 +518,8 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
     return ATTN_ERR_LAUNCH;
   const int grid = grid_for(p, g_dev[dev].num_sms);
   constexpr size_t smem = SmemPlan<D, NK, NV, kFp8, kFp4, kTmaO, kTable>::kBytes;
+  FwdParams pk = p;
+  pk.o_align32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // the API requires 16 only
   auto kernel = attn_fwd_kernel<D, NK, NV, kFp8, kPartial, kFp4, kTmaO, kTable, kPairTail>;
   if constexpr (kPairTail) {
     // clusters of two CTAs (the pairs of the split last round)
@@ -533,9 +535,9 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, p) != cudaSuccess) return ATTN_ERR_LAUNCH;
+    if (cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, pk) != cudaSuccess) return ATTN_ERR_LAUNCH;
   } else {
-    kernel<<<grid, kNumThreads, smem, static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mo, p);
+    kernel<<<grid, kNumThreads, smem, static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mo, pk);
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

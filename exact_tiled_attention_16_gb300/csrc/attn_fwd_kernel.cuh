@@ -118,7 +118,7 @@ static_assert(kRescaleThreshold + kFp8PScaleLog2 <= 15.0f, "FP8 P' would overflo
 // Every kPolyEvery-th pair of scores of a row would take its two exponentials
 // from the FMA pipe (exp2_poly2) instead of the special-function unit; 0 = all
 // on the SFU.  Measured on GB300 (doubled SFU ex2 rate), every share is slower:
-// cfg3-shaped causal d = 128 1659 TFLOP/s at 0, 1621 at 1/8, 1556 at 1/4, 1376
+// B1 H32 N16384 causal d = 128: 1659 TFLOP/s at 0, 1621 at 1/8, 1556 at 1/4, 1376
 // at 1/2; d = 64 1022 -> 994 -> 944 -> 741.  The polynomial costs about ten
 // FMA/ALU instructions per pair against two SFU issues, and the softmax is
 // bound by its instruction chain rather than by the SFU's throughput.
@@ -146,6 +146,7 @@ struct FwdParams {
   int blocks_per_split;
   int num_units;      // BH * num_pairs * num_splits
   int causal;
+  int o_align32;      // o is 32-byte aligned (set at launch)
   int order;          // unit order: kOrderHeads, kOrderZigzag or kOrderGroups (below)
   int group_heads;    // kOrderGroups: heads per group
   int sched_table;    // launched as a kTable instance (host bookkeeping)
@@ -1154,7 +1155,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
               tc_fence_before();
               mbar_arrive(b_o_free + 8 * t);
             }
-            if (row < p.Nq) {
+            // BF16: 32-byte stores when O allows them (a warp's store then fills
+            // whole 32-byte sectors of its 32 rows: B4 H16 N2048 d128 causal +3%); FP8
+            // measured no gain
+            if (!kFp8 && row < p.Nq && p.o_align32) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  w[e] = pack_bf16x2(__uint_as_float(oraw[16 * v + 2 * e]) * inv_l,
+                                     __uint_as_float(oraw[16 * v + 2 * e + 1]) * inv_l);
+                st_global_v8(dst + 8 * h + 2 * v, w);
+              }
+            } else if (row < p.Nq) {
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
                 uint32_t w[4];

@@ -141,25 +141,33 @@ def test_lse_optional():
 def test_no_writes_outside_outputs(causal, d):
     """O and LSE are written in place inside guard regions that must stay intact
     (non-causal launches store O with TMA, whose boxes are clipped at the ragged
-    tail N = 333 and at every head boundary; causal ones store rows directly)."""
+    tail N = 333 and at every head boundary; causal ones store rows directly, 32
+    bytes at a time when O is 32-byte aligned, else 16).  O is placed 32-byte
+    aligned and then 16 bytes off: the two results are the same bits."""
     import exact_tiled_attention_16_gb300._lib as L
     B, H, N = 1, 3, 333
     w = synth.make_bf16(B, H, N, d, causal, seed=61)
     q, k, v = to_device(w)
-    guard = 4096
-    o_buf = torch.full((B * H * N * d + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
-    l_buf = torch.full((B * H * N + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
-    o_view = o_buf[guard:guard + B * H * N * d]
-    l_view = l_buf[guard:guard + B * H * N]
-    rc = L.attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_view.data_ptr(), l_view.data_ptr(),
-                        B, H, N, d, causal, w.scale, torch.cuda.current_stream().cuda_stream)
-    assert rc == 0
-    torch.cuda.synchronize()
-    assert torch.isnan(o_buf[:guard].float()).all() and torch.isnan(o_buf[-guard:].float()).all()
-    assert torch.isnan(l_buf[:guard]).all() and torch.isnan(l_buf[-guard:]).all()
-    assert not torch.isnan(o_view.float()).any() and not torch.isnan(l_view).any()
-    assert_bf16_tol(compare_rows(w, o_view.view(B, H, N, d).float().cpu().numpy().astype(np.float64),
-                                 l_view.view(B, H, N).cpu().numpy().astype(np.float64)), "guarded")
+    results = []
+    for shift in (0, 8):  # elements: 0 and 16 bytes past a 32-byte boundary
+        guard = 4096
+        o_buf = torch.full((B * H * N * d + 2 * guard + shift,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        l_buf = torch.full((B * H * N + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+        assert o_buf.data_ptr() % 256 == 0
+        o_view = o_buf[guard + shift:guard + shift + B * H * N * d]
+        l_view = l_buf[guard:guard + B * H * N]
+        assert (o_view.data_ptr() % 32 == 0) == (shift == 0)
+        rc = L.attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_view.data_ptr(), l_view.data_ptr(),
+                            B, H, N, d, causal, w.scale, torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert torch.isnan(o_buf[:guard + shift].float()).all() and torch.isnan(o_buf[-guard:].float()).all()
+        assert torch.isnan(l_buf[:guard]).all() and torch.isnan(l_buf[-guard:]).all()
+        assert not torch.isnan(o_view.float()).any() and not torch.isnan(l_view).any()
+        assert_bf16_tol(compare_rows(w, o_view.view(B, H, N, d).float().cpu().numpy().astype(np.float64),
+                                     l_view.view(B, H, N).cpu().numpy().astype(np.float64)), f"guarded, shift {shift}")
+        results.append(o_view.clone())
+    assert torch.equal(results[0].view(torch.int16), results[1].view(torch.int16))
 
 
 def test_invalid_arguments_launch_nothing():
