@@ -630,7 +630,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   const size_t smem = BwdSmem<D, RA, RB>::kBytes;
   attn_bwd_dq_kernel<D, RA, RB><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-  attn_bwd_dkdv_kernel<D, RA, RB><<<grid, kBwdThreads, smem, st>>>(mq, mk, mv, mdo, bp);
+  attn_bwd_dkdv_kernel<D, RA, RB><<<grid, kDkdvThreads, smem, st>>>(mq, mk, mv, mdo, bp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 // The pipeline of the host-buffer entry points: chunks of whole heads through two

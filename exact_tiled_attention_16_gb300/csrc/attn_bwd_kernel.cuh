@@ -18,10 +18,12 @@
 //   bwd_dkdv   unit = 128 keys of one (b, h); loops over query blocks:
 //              S^T = K Q^T and dP^T = V dO^T (SS MMAs), P^T and dS^T into TMEM,
 //              dV += P^T dO and dK += dS^T Q (TS MMAs)
-// Each CTA: warps 0-7 compute in two warpgroups -- thread t of warpgroup h owns
-// TMEM lane t (one row of the tile) and columns 64h..64h+63 of each 128-column
-// tile, and writes its bf16 result into the first 32 of those columns -- warp 8
-// is the TMA producer, warp 9 the MMA warp (one elected lane issues; TMEM owner).
+// Each CTA of the dQ pass: warps 0-7 compute in two warpgroups -- thread t of
+// warpgroup h owns TMEM lane t (one row of the tile) and columns 64h..64h+63 of
+// each 128-column tile, and writes its bf16 result into the first 32 of those
+// columns -- warp 8 is the TMA producer, warp 9 the MMA warp (one elected lane
+// issues; TMEM owner).  The dK/dV pass does the same with four warpgroups of 32
+// columns (warps 0-15), its producer and MMA warps 16 and 17.
 // dQ and dK/dV are separate passes, so no atomics are needed and the result is
 // deterministic (the two S-type products are computed in both passes).
 #pragma once
@@ -39,6 +41,17 @@ constexpr int kBwdComputeThreads = 256;
 constexpr int kBwdThreads = 320;
 constexpr int kBwdProducerWarp = 8;
 constexpr int kBwdMmaWarp = 9;
+// The dK/dV pass: four compute warpgroups (a quarter of every tile's 128 columns
+// each), then the TMA producer warp and the MMA warp.  Four warps per sub-partition
+// overlap the recomputed softmax's chain of TMEM load, arithmetic and TMEM store,
+// which bound the pass with two (same results bit for bit; the backward of B16 H16
+// N4096 d64 +6.5%, of B1 H32 N16384 d128 causal +3.7%); the dQ pass gained nothing
+// from four and keeps two.
+constexpr int kDkdvWarpgroups = 4;
+constexpr int kDkdvComputeThreads = 128 * kDkdvWarpgroups;
+constexpr int kDkdvThreads = kDkdvComputeThreads + 64;
+constexpr int kDkdvProducerWarp = kDkdvComputeThreads / 32;
+constexpr int kDkdvMmaWarp = kDkdvProducerWarp + 1;
 
 struct BwdParams {
   const __nv_bfloat16* o;     // [BH, N, D]   (prep)
@@ -112,19 +125,21 @@ struct BwdSmem {
 };
 
 // acc (+)= A B with A = 128 x 128 bf16 in TMEM (two keys per column) laid out as
-// the compute warpgroups write it: keys 0..63 in columns a_region + 0..31,
-// keys 64..127 in a_region + 64..95; B = 128 rows x D at b_base, MN-major.
+// kWG compute warpgroups write it: warpgroup w's 128 / kWG keys in the first half
+// of its own 128 / kWG columns (two warpgroups: keys 0..63 in columns a_region +
+// 0..31, keys 64..127 in a_region + 64..95); B = 128 rows x D at b_base, MN-major.
 // (Descriptors as 32-bit low words: step kk adds its byte offset >> 4 to the
 // address field, which never carries since shared memory stays below 2^18.)
-template <typename L>
+template <typename L, int kWG = 2>
 __device__ __forceinline__ void bwd_issue_ts(uint32_t acc, uint32_t a_region, uint32_t b_base, uint32_t idesc,
                                              bool accumulate) {
   const uint32_t b0 = sdesc_lo(b_base, L::kChunkBytes);
   constexpr uint32_t hi = sdesc_hi_sw128(1024);
+  constexpr int kSteps = 8 / kWG;  // 16-key MMA steps per warpgroup
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_f16_ts_w(acc, a_region + (kk >> 2) * 64 + (kk & 3) * 8, b0 + ((kk * 16 * 128) >> 4), hi, idesc,
-                 (accumulate || kk > 0) ? 1u : 0u);
+    mma_f16_ts_w(acc, a_region + (kk / kSteps) * (128 / kWG) + (kk % kSteps) * 8, b0 + ((kk * 16 * 128) >> 4),
+                 hi, idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // C = A B^T with A, B 128 x D K-major bf16 tiles.
@@ -139,15 +154,17 @@ __device__ __forceinline__ void bwd_issue_ss(uint32_t c_tmem, uint32_t a_base, u
   }
 }
 
-// One thread's half of an accumulator row (D/2 fp32 TMEM columns) -> bf16 at dst.
-template <int D>
-__device__ __forceinline__ void bwd_store_half_row(uint32_t taddr, __nv_bfloat16* dst, bool valid) {
-  constexpr int kCols = D / 2;
+// One thread's part of an accumulator row (kCols fp32 TMEM columns) -> bf16 at dst.
+template <int kCols>
+__device__ __forceinline__ void bwd_store_row_part(uint32_t taddr, __nv_bfloat16* dst, bool valid) {
+  static_assert(kCols == 16 || kCols == 32 || kCols == 64, "16, 32 or 64 columns");
   uint32_t a[kCols];
   if constexpr (kCols == 64) {
     tmem_ld64_wait(taddr, a);
-  } else {
+  } else if constexpr (kCols == 32) {
     tmem_ld32_wait(taddr, a);
+  } else {
+    tmem_ld16_wait(taddr, a);
   }
   if (valid) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -486,7 +503,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       if (!(ok = warp_wait(b_dq_done, units & 1, abort_flag, tmo, p.err, 62))) break;
       tc_fence_after();
       const bool valid = row < p.N;
-      bwd_store_half_row<D>(tmem + lane_addr + kDQ + (D / 2) * wg,
+      bwd_store_row_part<D / 2>(tmem + lane_addr + kDQ + (D / 2) * wg,
                             p.dq + (static_cast<size_t>(bh) * p.N + (valid ? row : 0)) * D + (D / 2) * wg, valid);
       tc_fence_before();
       mbar_arrive(b_dq_free);
@@ -506,7 +523,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 // warpgroup's columns), dP^T at 128 (dS^T likewise), dV at 256, dK at 256 + D.
 // ---------------------------------------------------------------------------
 template <int D, int RA, int RB>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
                      const BwdParams p) {
@@ -537,11 +554,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     mbar_init(b_kv_full, 1);
     mbar_init(b_kv_empty, 1);
     mbar_init(b_st_full, 1);
-    mbar_init(b_p_ready, kBwdComputeThreads);
+    mbar_init(b_p_ready, kDkdvComputeThreads);
     mbar_init(b_dpt_full, 1);
-    mbar_init(b_ds_ready, kBwdComputeThreads);
+    mbar_init(b_ds_ready, kDkdvComputeThreads);
     mbar_init(b_acc_done, 1);
-    mbar_init(b_acc_free, kBwdComputeThreads);
+    mbar_init(b_acc_free, kDkdvComputeThreads);
     mbar_init(b_drain, 1);
     for (int s = 0; s < RA; ++s) {
       mbar_init(rg.a_full + 8 * s, 1);
@@ -554,7 +571,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kBwdMmaWarp) {
+  if (warp == kDkdvMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -571,7 +588,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     i0 = p.causal ? kb : 0;
   };
 
-  if (warp == kBwdProducerWarp) {
+  if (warp == kDkdvProducerWarp) {
     if (lane == 0) {
       // K and V are read by this unit only; Q and dO by every key block of the head
       const uint64_t pol_once = l2_policy_evict_first(), pol_ring = l2_policy_evict_last();
@@ -609,7 +626,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       }
       bwd_producer_drain<RA, RB>(ok, ga, gb, units, rg, b_kv_full, b_kv_empty, abort_flag, tmo, p.err, 73);
     }
-  } else if (warp == kBwdMmaWarp) {
+  } else if (warp == kDkdvMmaWarp) {
     {  // whole warp, warp-uniform; one elected lane issues each MMA and commit
       constexpr uint32_t idesc_ss = make_idesc(kBlockM, kBlockN, 1, false);
       constexpr uint32_t idesc_acc = make_idesc(kBlockM, D, 1, true);  // B = dO or Q, MN-major
@@ -642,7 +659,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           ++p_iter;
           if (b == 0 && units > 0 && !(ok = ATTN_BWD_WAIT_W(b_acc_free, (units - 1) & 1, 84))) break;
           tc_fence_after();
-          bwd_issue_ts<L>(tmem + kDV, tmem + kS, sDO + (gb % RB) * L::kTileBytes, idesc_acc, b > 0);
+          bwd_issue_ts<L, kDkdvWarpgroups>(tmem + kDV, tmem + kS, sDO + (gb % RB) * L::kTileBytes, idesc_acc, b > 0);
           mma_commit(rg.b_empty + 8 * (gb % RB));
           if (b + 1 < n) {
             // S^T_{b+1} overwrites P^T_b, which the dV product above has consumed
@@ -655,7 +672,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           if (!(ok = ATTN_BWD_WAIT_W(b_ds_ready, ds_iter & 1, 86))) break;
           ++ds_iter;
           tc_fence_after();
-          bwd_issue_ts<L>(tmem + kDK, tmem + kDP, sQ + (gb % RA) * L::kTileBytes, idesc_acc, b > 0);
+          bwd_issue_ts<L, kDkdvWarpgroups>(tmem + kDK, tmem + kDP, sQ + (gb % RA) * L::kTileBytes, idesc_acc, b > 0);
           mma_commit(rg.a_empty + 8 * (gb % RA));
           if (b == n - 1) {
             mma_commit(b_acc_done);
@@ -677,10 +694,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     }
   } else {
     // ----------------------------------------------------------- compute
-    const int wg = warp >> 2;         // column half of every tile
+    constexpr int kQ = kBlockM / kDkdvWarpgroups;  // this warpgroup's queries (columns) of a tile
+    const int wg = warp >> 2;         // column quarter of every tile
     const int t = threadIdx.x & 127;  // key within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + kS + 64 * wg, tP = tmem + lane_addr + kDP + 64 * wg;
+    const uint32_t tS = tmem + lane_addr + kS + kQ * wg, tP = tmem + lane_addr + kDP + kQ * wg;
     const float2 cs2 = make_float2(p.scale_log2, p.scale_log2);
     const float2 sc2 = make_float2(p.scale, p.scale);
     uint32_t st_iter = 0, dp_iter = 0;
@@ -694,24 +712,24 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       unit(u, bh, kb, i0);
       const int key = kb * kBlockN + t;
       for (int i = i0; i < T; ++i) {
-        // this warpgroup's 64 queries of block i: -lse log2e and -scale D, from
+        // this warpgroup's kQ queries of block i: -lse log2e and -scale D, from
         // the padded workspace (16-byte aligned; -inf and 0 past N)
-        const size_t voff = static_cast<size_t>(bh) * p.Npad + i * kBlockM + 64 * wg;
+        const size_t voff = static_cast<size_t>(bh) * p.Npad + i * kBlockM + kQ * wg;
         const float4* nl4 = reinterpret_cast<const float4*>(p.nlse2 + voff);
         const float4* nd4 = reinterpret_cast<const float4*>(p.nds + voff);
-        float4 nl[16];
+        float4 nl[kQ / 4];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) nl[c] = __ldg(nl4 + c);
+        for (int c = 0; c < kQ / 4; ++c) nl[c] = __ldg(nl4 + c);
         if (!(ok = warp_wait(b_st_full, st_iter & 1, abort_flag, tmo, p.err, 90))) break;
         ++st_iter;
         tc_fence_after();
-        uint32_t sraw[64];
-        tmem_ld64_wait(tS, sraw);
+        uint32_t sraw[kQ];
+        tmem_ld32_wait(tS, sraw);
         // P^T[key][q] = 2^(s scale log2e - lse_q log2e); zero for queries before
         // the key (causal diagonal block) and past N (lse = +inf)
-        uint32_t pk[32];
+        uint32_t pk[kQ / 2];
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < kQ; c += 4) {
           const float4 l = nl[c / 4];
           const float2 e0 = ffma2(make_float2(__uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1])), cs2,
                                   make_float2(l.x, l.y));
@@ -721,29 +739,29 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           pk[c / 2 + 1] = pack_bf16x2(ex2_approx(e1.x), ex2_approx(e1.y));
         }
         if (p.causal && i == kb) {
-          // query 64 wg + c is visible to key t iff 64 wg + c >= t
-          const int first = t - 64 * wg;
+          // query kQ wg + c is visible to key t iff kQ wg + c >= t
+          const int first = t - kQ * wg;
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
+          for (int c = 0; c < kQ; c += 2) {
             const uint32_t lo = c >= first ? 0x0000ffffu : 0u, hi = c + 1 >= first ? 0xffff0000u : 0u;
             pk[c / 2] &= lo | hi;
           }
         }
-        tmem_st32(tS, pk);
+        tmem_st16(tS, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_p_ready);
-        float4 nd[16];
+        float4 nd[kQ / 4];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) nd[c] = __ldg(nd4 + c);
+        for (int c = 0; c < kQ / 4; ++c) nd[c] = __ldg(nd4 + c);
         if (!(ok = warp_wait(b_dpt_full, dp_iter & 1, abort_flag, tmo, p.err, 91))) break;
         ++dp_iter;
         tc_fence_after();
-        uint32_t dpr[64];
-        tmem_ld64_wait(tP, dpr);
+        uint32_t dpr[kQ];
+        tmem_ld32_wait(tP, dpr);
         // dS^T scale = P^T (scale dP^T - scale D), from the bf16 P^T of the dV product
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < kQ; c += 4) {
           const float4 d = nd[c / 4];
           const float2 x0 = ffma2(make_float2(__uint_as_float(dpr[c]), __uint_as_float(dpr[c + 1])), sc2,
                                   make_float2(d.x, d.y));
@@ -754,7 +772,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           pk[c / 2] = pack_bf16x2(ds0.x, ds0.y);
           pk[c / 2 + 1] = pack_bf16x2(ds1.x, ds1.y);
         }
-        tmem_st32(tP, pk);
+        tmem_st16(tP, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_ds_ready);
@@ -763,9 +781,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       if (!(ok = warp_wait(b_acc_done, units & 1, abort_flag, tmo, p.err, 92))) break;
       tc_fence_after();
       const bool valid = key < p.N;
-      const size_t kidx = (static_cast<size_t>(bh) * p.N + (valid ? key : 0)) * D + (D / 2) * wg;
-      bwd_store_half_row<D>(tmem + lane_addr + kDV + (D / 2) * wg, p.dv + kidx, valid);
-      bwd_store_half_row<D>(tmem + lane_addr + kDK + (D / 2) * wg, p.dk + kidx, valid);
+      constexpr int kC = D / kDkdvWarpgroups;  // this warpgroup's columns of dK and dV
+      const size_t kidx = (static_cast<size_t>(bh) * p.N + (valid ? key : 0)) * D + kC * wg;
+      bwd_store_row_part<kC>(tmem + lane_addr + kDV + kC * wg, p.dv + kidx, valid);
+      bwd_store_row_part<kC>(tmem + lane_addr + kDK + kC * wg, p.dk + kidx, valid);
       tc_fence_before();
       mbar_arrive(b_acc_free);
       ++units;
@@ -773,7 +792,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kBwdMmaWarp) {
+  if (warp == kDkdvMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
