@@ -7,6 +7,8 @@ import os
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
@@ -39,6 +41,24 @@ def test_kernel_instance_follows_the_instance_table():
             == "attn::attn_fwd_kernel<128, 3, 3, 1, 0, 0, 0, 0, 1>")
     assert (bench.kernel_instance("e4m3_e2m1", 128, pair_tail=True)
             == "attn::attn_fwd_kernel<128, 4, 4, 1, 0, 1, 0, 0, 0>")
+
+
+def test_custom_workloads():
+    """--custom B,H,N,d,causal[,e4m3]: a seeded BF16 workload, or a block-scaled e4m3
+    one with cfg5's recipe, of that shape; --all carries the FP8 shape whose last
+    round is split over CTA pairs."""
+    import argparse
+    import numpy as np
+    w = bench.make_workload(argparse.Namespace(custom="1,2,300,64,1", workload="cfg3"))
+    assert (w.dtype, w.B, w.H, w.N, w.d, w.causal) == ("bf16", 1, 2, 300, 64, True)
+    assert w.name == "custom_B1H2N300d64c"
+    w = bench.make_workload(argparse.Namespace(custom="1,2,300,128,0,e4m3", workload="cfg3"))
+    assert (w.dtype, w.B, w.H, w.N, w.d, w.causal) == ("e4m3", 1, 2, 300, 128, False)
+    assert w.name == "custom_B1H2N300d128n_e4m3"
+    assert w.q.dtype == np.uint8 and w.q_scale.shape == (1, 2, 3)
+    with pytest.raises(SystemExit):
+        bench.make_workload(argparse.Namespace(custom="1,2,300,128,0,fp16", workload="cfg3"))
+    assert "custom:1,16,8192,128,0,e4m3" in bench.ALL_WORKLOADS
 
 
 def test_kernel_hash_covers_every_cuda_source(tmp_path, monkeypatch):
