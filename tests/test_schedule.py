@@ -189,7 +189,7 @@ def test_fp8_pair_tail(shape):
     full, rem = divmod(U, G)
     want = 0 < rem <= G // 2 and N >= 48 * 128
     assert info["pair_tail"] == int(want)
-    units = np.concatenate([seq[seq >= 0]])
+    units = seq[seq >= 0]
     assert np.array_equal(np.sort(units), np.arange(U))
     if want:
         assert np.array_equal(seq[1::2, full][:rem], -3 - np.arange(full * G, U))
